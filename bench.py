@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Throughput of the Gated DeltaNet layer on GB300: one JSON line on stdout.
+
+Headline ("step" = one decode call over a batch of 64 sequences, every step of
+the layer in one kernel): B=64, H_k=16, H_v=32, d_k=d_v=128, K=4, bf16 qkv,
+carried fp32 state, fresh seeded inputs each step.  Two state sets rotate so
+that each step reads its state from HBM (2 x 134 MB > the 126 MB L2).
+
+Also reported on the same line (N=1 only): the L=8192 prefill, the packed
+varlen prefill (16 sequences, lengths U{256..2048}) and the B=32, L=4 MTP
+verify + commit.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+page describes no GPU implementation to compare with).  Under torchrun, ranks
+run independent replicas (the layer has no cross-sequence exchange): rank 0
+prints, value = tokens of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN layer tokens/s (decode B=64, prefill L=8192); % of GB300 HBM roofline"
+B_DECODE, N_INPUT_STEPS = 64, 256
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def _source_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "gated_deltanet_linear_causal_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_key, sources):
+    """Per-launch DRAM bytes from the committed ncu summary, or None if the kernel's
+    sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("source_sha") != _source_sha(sources):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the GPU is under the bench's load."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc = index, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def _to_dev(arr, dev):
+    import numpy as np
+    import torch
+    arr = np.ascontiguousarray(arr)
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(arr).to(dev)
+
+
+def _pinned(arr):
+    import numpy as np
+    import torch
+    arr = np.ascontiguousarray(arr)
+    t = torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16) if arr.dtype == np.uint16 else torch.from_numpy(arr)
+    return t.pin_memory()
+
+
+# ---------------------------------------------------------------------------
+# Workloads on the GPU
+# ---------------------------------------------------------------------------
+
+def decode_bytes(shape, B):
+    """Algorithmic HBM bytes of one decode call: S read+write, qkv, conv state read+write,
+    output, conv weight, gate and beta."""
+    S = B * shape.num_v_heads * shape.head_k_dim * shape.head_v_dim * 4
+    return (2 * S + B * shape.D * 2 + 2 * B * shape.D * (shape.conv_kernel - 1) * 2 +
+            B * shape.num_v_heads * shape.head_v_dim * 4 + shape.D * shape.conv_kernel * 2 +
+            2 * B * shape.num_v_heads * 4)
+
+
+def prefill_bytes(shape, cu, random_state):
+    """qkv in, fp32 output, gate and beta, conv weight, states (final write; plus the
+    initial read when the sequences start from a given state)."""
+    import numpy as np
+    T, N = int(cu[-1]), len(cu) - 1
+    S = N * shape.num_v_heads * shape.head_k_dim * shape.head_v_dim * 4
+    conv = N * shape.D * (shape.conv_kernel - 1) * 2
+    return (T * shape.D * 2 + T * shape.num_v_heads * shape.head_v_dim * 4 + 2 * T * shape.num_v_heads * 4 +
+            shape.D * shape.conv_kernel * 2 + (2 if random_state else 1) * (S + conv))
+
+
+def verify_bytes(shape, B, L):
+    S = B * shape.num_v_heads * shape.head_k_dim * shape.head_v_dim * 4
+    conv = B * shape.D * (shape.conv_kernel - 1) * 2
+    return (S + L * S + conv + L * conv + B * L * shape.D * 2 + B * L * shape.num_v_heads * shape.head_v_dim * 4 +
+            2 * B * L * shape.num_v_heads * 4 + shape.D * shape.conv_kernel * 2)
+
+
+def run_decode(args, dev, dist, rank, world):
+    import numpy as np
+    import torch
+    from gated_deltanet_linear_causal_gb300 import binding as gb, synth
+    shape = synth.PRODUCTION
+    cfg = gb.make_config(16, 32, 128, 128, 4, True, 1e-6, "bf16")
+    st = synth.decode_state(2 + 1000 * rank, B_DECODE, shape)
+    n_in = min(N_INPUT_STEPS, max(args.steps, 1) + args.warmup)
+    steps = [synth.decode_step(2 + 1000 * rank, s, B_DECODE, shape) for s in range(n_in)]
+    qkv = torch.stack([_to_dev(s["qkv"], dev) for s in steps])
+    gate = torch.stack([_to_dev(s["gate"], dev) for s in steps])
+    beta = torch.stack([_to_dev(s["beta"], dev) for s in steps])
+    w = _to_dev(st["conv_weight"], dev)
+    per_step = decode_bytes(shape, B_DECODE)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, math.ceil(2 * l2 / per_step))
+    S = [_to_dev(st["ssm_state"], dev) for _ in range(R)]
+    conv = [_to_dev(st["conv_state"], dev) for _ in range(R)]
+    out = torch.empty(B_DECODE, 32, 128, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j, r = i % n_in, i % R
+        gb.gdn_forward_decode(cfg, B_DECODE, qkv[j], w, gate[j], beta[j], conv[r], S[r], out)
+
+    for i in range(args.warmup):
+        step(i)
+    # untimed soak (~1 s) so the clock sampler sees the GPU under this load
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + 1.0
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(64):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = B_DECODE * args.steps * world
+    value = tokens / (ms / 1e3)
+    launch_us = ms * 1e3 / args.steps
+
+    # end to end through the public binding: pinned host inputs in, output back to pinned host
+    h_qkv = [_pinned(s["qkv"]) for s in steps]
+    h_gate = [_pinned(s["gate"]) for s in steps]
+    h_beta = [_pinned(s["beta"]) for s in steps]
+    d_qkv, d_gate, d_beta = torch.empty_like(qkv[0]), torch.empty_like(gate[0]), torch.empty_like(beta[0])
+    h_out = torch.empty(B_DECODE, 32, 128).pin_memory()
+
+    def e2e_step(i):
+        j, r = i % n_in, i % R
+        d_qkv.copy_(h_qkv[j], non_blocking=True)
+        d_gate.copy_(h_gate[j], non_blocking=True)
+        d_beta.copy_(h_beta[j], non_blocking=True)
+        gb.gdn_forward_decode(cfg, B_DECODE, d_qkv, w, d_gate, d_beta, conv[r], S[r], out)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = h_qkv[0].numel() * 2 + h_gate[0].numel() * 4 + h_beta[0].numel() * 4
+    d2h = h_out.numel() * 4
+    return dict(ms=ms, value=value, launch_us=launch_us, bytes=per_step, rotation=R, clocks=clk,
+                e2e=dict(value=tokens / (ms_e2e / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
+                         d2h_bytes_per_step=d2h), inputs=dict(steps=steps, state=st))
+
+
+def _time_calls(fn, reps, flush):
+    import torch
+    times = []
+    for _ in range(reps):
+        flush()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times), times
+
+
+def run_prefill(dev, x, variant, reps=5):
+    import numpy as np
+    import torch
+    from gated_deltanet_linear_causal_gb300 import binding as gb, synth
+    shape = x["shape"]
+    cfg = gb.make_config(shape.num_k_heads, shape.num_v_heads, shape.head_k_dim, shape.head_v_dim, 4, True, 1e-6,
+                         "bf16")
+    cu = x["cu_seqlens"]
+    N, T = len(cu) - 1, int(cu[-1])
+    cu_d = _to_dev(cu, dev)
+    qkv, w = _to_dev(x["qkv"], dev), _to_dev(x["conv_weight"], dev)
+    gate, beta = _to_dev(x["gate"], dev), _to_dev(x["beta"], dev)
+    conv0, S0 = _to_dev(x["conv_state"], dev), _to_dev(x["ssm_state"], dev)
+    conv, S = conv0.clone(), S0.clone()
+    out = torch.empty(T, shape.num_v_heads, shape.head_v_dim, device=dev)
+    ws = torch.empty(max(1, gb.gdn_prefill_workspace_size(cfg, N, T, variant)), dtype=torch.uint8, device=dev)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():  # restore the initial states and push the L2 out (256 MiB write)
+        conv.copy_(conv0)
+        S.copy_(S0)
+        scratch.zero_()
+
+    def call():
+        gb.gdn_forward_prefill(cfg, N, cu_d, cu, qkv, w, gate, beta, conv, S, out, variant, ws)
+
+    call()
+    med, times = _time_calls(call, reps, flush)
+    return med, times
+
+
+def run_verify(dev, x, reps=10):
+    import torch
+    from gated_deltanet_linear_causal_gb300 import binding as gb
+    shape = x["shape"]
+    B, L = x["qkv"].shape[0], x["qkv"].shape[2]
+    cfg = gb.make_config(16, 32, 128, 128, 4, True, 1e-6, "bf16")
+    d = {k: _to_dev(x[k], dev) for k in ("qkv", "conv_weight", "gate", "beta", "conv_state", "ssm_state", "accepted")}
+    csnap = torch.empty(B, L, shape.D, 3, dtype=torch.bfloat16, device=dev)
+    ssnap = torch.empty(B, L, 32, 128, 128, device=dev)
+    out = torch.empty(B, L, 32, 128, device=dev)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def verify():
+        gb.gdn_forward_verify(cfg, B, L, d["qkv"], d["conv_weight"], d["gate"], d["beta"], d["conv_state"],
+                              d["ssm_state"], csnap, ssnap, out)
+
+    def commit():
+        gb.gdn_verify_commit(cfg, B, L, d["accepted"], csnap, ssnap, d["conv_state"], d["ssm_state"])
+
+    verify()
+    mv, _ = _time_calls(verify, reps, lambda: scratch.zero_())
+    mc, _ = _time_calls(commit, reps, lambda: (verify(), scratch.zero_()))
+    return mv, mc
+
+
+# ---------------------------------------------------------------------------
+# fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_decode_rate(steps, state, budget_s, max_steps):
+    """Oracle decode steps of the B=64 workload (all sequences, all heads) until the
+    time budget is spent; returns (tokens/s, sample description)."""
+    import oracle
+    from gated_deltanet_linear_causal_gb300 import synth
+    shape = synth.PRODUCTION
+    ocfg = oracle.Cfg(16, 32, 128, 128, 4, True, 1e-6)
+    conv = synth.as_f64(state["conv_state"], "bf16")
+    S = state["ssm_state"].astype("float64")
+    w = synth.as_f64(state["conv_weight"], "bf16")
+    t0 = time.perf_counter()
+    tokens, n = 0, 0
+    seqs_per_chunk = 8
+    while n < max_steps:
+        s = steps[n % len(steps)]
+        qkv = synth.as_f64(s["qkv"], "bf16")
+        for b0 in range(0, B_DECODE, seqs_per_chunk):
+            idx = list(range(b0, b0 + seqs_per_chunk))
+            _, c_new, S_new = oracle.decode(ocfg, qkv, w, s["gate"], s["beta"], conv, S, batch_index=idx)
+            conv[idx], S[idx] = c_new, S_new
+            tokens += len(idx)
+            if time.perf_counter() - t0 > budget_s:
+                break
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return tokens / dt, f"{tokens} decode tokens ({n} step(s) of the B=64 workload, all 32 heads) in {dt:.1f} s"
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-secondary", action="store_true", help="headline decode only")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        return main_reference(args)
+
+    import torch
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from gated_deltanet_linear_causal_gb300 import binding as gb, synth
+    gb.load()
+    peaks = _peaks()
+    dec = run_decode(args, dev, dist, rank, world)
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    shape = synth.PRODUCTION
+    achieved = dec["bytes"] / (dec["launch_us"] * 1e-6) / 1e9
+    sources = ["gdn_step.cu", "gdn_common.cuh"]
+    line = {
+        "metric": METRIC, "value": round(dec["value"], 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms"] / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "decode B=64, H_k=16, H_v=32, d_k=d_v=128, K=4, bf16 qkv, fp32 state, "
+                               "fresh seeded inputs per step",
+                   "global_batch": B_DECODE * world, "seq_len": 1, "parallelism": f"replicas{world}",
+                   "io": "bf16", "l2": f"inputs larger than L2: {dec['rotation']} rotating state sets of "
+                                         f"{dec['bytes'] / 1e6:.1f} MB per step"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("decode_b64", sources),
+                     "kernel": "step_kernel<bf16,128,in_place>", "algorithmic_bytes_per_launch": dec["bytes"],
+                     "launch_us": round(dec["launch_us"], 2), "peak_source": peaks["source"]},
+        "e2e": dec["e2e"], "gpu_launches": args.steps, "clocks": dec["clocks"],
+    }
+    if world == 1:
+        v, sample = oracle_decode_rate(dec["inputs"]["steps"], dec["inputs"]["state"], args.cpu_budget, args.steps)
+        line["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": sample}
+    if world == 1 and not args.no_secondary:
+        sec = {}
+        x = synth.long_prefill(seed=3)
+        med, times = run_prefill(dev, x, gb.GDN_PREFILL_RESIDENT)
+        nb = prefill_bytes(shape, x["cu_seqlens"], False)
+        sec["prefill_L8192"] = {"variant": "resident", "tokens_per_s": round(8192 / (med / 1e3), 1),
+                                "ms": round(med, 4), "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
+        del x
+        x = synth.varlen_prefill(seed=4)
+        med, _ = run_prefill(dev, x, gb.GDN_PREFILL_RESIDENT)
+        T = int(x["cu_seqlens"][-1])
+        nb = prefill_bytes(shape, x["cu_seqlens"], True)
+        sec["prefill_varlen16"] = {"variant": "resident", "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
+                                   "ms": round(med, 4),
+                                   "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                   "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
+        del x
+        x = synth.verify_block(seed=5)
+        mv, mc = run_verify(dev, x)
+        nb = verify_bytes(shape, 32, 4)
+        sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4),
+                                "roofline_frac": round(nb / (mv / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": nb, "commit_ms": round(mc, 4), "cold_l2": True}
+        line["secondary"] = sec
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main_reference(args):
+    """The fp64 oracle, single-threaded, on this host's cores, on the decode workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gated_deltanet_linear_causal_gb300 import synth
+    import oracle
+    oracle.build()
+    st = synth.decode_state(2, B_DECODE, synth.PRODUCTION)
+    steps = [synth.decode_step(2, s, B_DECODE, synth.PRODUCTION) for s in range(4)]
+    budget = max(2.0, min(args.cpu_budget, 8.0))
+    t0 = time.perf_counter()
+    v, sample = oracle_decode_rate(steps, st, budget, max(1, args.steps))
+    total = time.perf_counter() - t0
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(B_DECODE / v * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode B=64, H_k=16, H_v=32, d_k=d_v=128, K=4, bf16 qkv (fp64 oracle)",
+                       "global_batch": B_DECODE, "seq_len": 1, "parallelism": "host, 1 thread"},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(total, 2)}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,72 @@
+// gdn_internal.h -- launch interfaces between the C-ABI layer (gdn_api.cu) and
+// the kernels.  Arguments here are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Geometry shared by every launch.
+struct Geom {
+    int Hk, Hv, dk, dv, K, D, f;  // f = Hv / Hk
+    int use_l2;
+    float eps;
+    float q_scale;  // 1/sqrt(dk) rounded to fp32
+    int io_bf16;    // 1: bf16 storage, 0: fp32 storage
+};
+
+// Decode (in place, L = 1) and verify (snapshots, L tokens) share one kernel.
+struct StepArgs {
+    Geom g;
+    int B, L;
+    const void* qkv;      // [B, D, L]
+    const void* w;        // [D, K]
+    const float* gate;    // [B, L, Hv]
+    const float* beta;    // [B, L, Hv]
+    const void* conv_in;  // [B, D, K-1]
+    const float* S_in;    // [B, Hv, dk, dv]
+    void* conv_out;       // decode: conv_in; verify: [B, L, D, K-1]
+    float* S_out;         // decode: S_in;    verify: [B, L, Hv, dk, dv]
+    float* out;           // [B, L, Hv, dv]
+};
+cudaError_t launch_step(const StepArgs& a, bool in_place, cudaStream_t stream);
+
+struct CommitArgs {
+    int B, L;
+    size_t conv_bytes;    // bytes of one sequence's conv state
+    size_t ssm_floats;    // floats of one sequence's recurrent state
+    int conv_vec16;       // conv bytes and both conv pointers allow 16-byte copies
+    const int32_t* accepted;
+    const void* conv_snap;
+    const float* ssm_snap;
+    void* conv_state;
+    float* ssm_state;
+    int32_t* status;
+};
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream);
+
+struct PrefillArgs {
+    Geom g;
+    int N;                     // sequences
+    int T;                     // packed tokens
+    int max_len;               // longest sequence
+    const int32_t* cu;         // device [N+1]
+    const int32_t* cu_host;    // host [N+1]
+    const void* qkv;           // [D, T]
+    const void* w;             // [D, K]
+    const float* gate;         // [T, Hv]
+    const float* beta;         // [T, Hv]
+    void* conv_state;          // [N, D, K-1]
+    float* ssm_state;          // [N, Hv, dk, dv]
+    float* out;                // [T, Hv, dv]
+    void* ws;                  // workspace
+    size_t ws_bytes;
+};
+size_t prefill_resident_workspace(const Geom& g, int N, long long T);
+cudaError_t launch_prefill_resident(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,64 @@
+"""Decode (L = 1, states in place) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_causal_gb300 import binding as gb
+from gated_deltanet_linear_causal_gb300 import synth
+from gdn_testutil import assert_parity, configs, device, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_decode_steps(shape, io, batch, steps, seed, use_l2=True, conv_kernel=None):
+    if conv_kernel is not None:
+        shape = synth.Shape(shape.num_k_heads, shape.num_v_heads, shape.head_k_dim, shape.head_v_dim, conv_kernel)
+    dev = device()
+    cfg, ocfg = configs(shape, io, use_l2)
+    st = synth.decode_state(seed, batch, shape)
+    conv_w = st["conv_weight"] if io == "bf16" else synth.bf16_bits_to_f32(st["conv_weight"])
+    conv0 = st["conv_state"] if io == "bf16" else synth.bf16_bits_to_f32(st["conv_state"])
+    w_d, conv_d, S_d = to_dev(conv_w, dev), to_dev(conv0, dev), to_dev(st["ssm_state"], dev)
+    conv_r, S_r = f64(conv0), st["ssm_state"].astype(np.float64)
+    out = torch.empty(batch, shape.num_v_heads, shape.head_v_dim, device=dev)
+    for step in range(steps):
+        d = synth.decode_step(seed, step, batch, shape)
+        qkv = d["qkv"] if io == "bf16" else synth.bf16_bits_to_f32(d["qkv"])
+        gb.gdn_forward_decode(cfg, batch, to_dev(qkv, dev), w_d, to_dev(d["gate"], dev), to_dev(d["beta"], dev),
+                              conv_d, S_d, out)
+        o_r, conv_r, S_r = oracle.decode(ocfg, f64(qkv), f64(conv_w), d["gate"], d["beta"], conv_r, S_r)
+        torch.cuda.synchronize()
+        assert_parity(f64(out), o_r, what=f"step {step} output")
+    assert_parity(f64(out), o_r, f64(S_d), S_r, what="final")
+    assert np.array_equal(f64(conv_d), conv_r), "conv state must be the exact raw inputs"
+
+
+def test_decode_oracle_scale_f32():
+    _run_decode_steps(synth.ORACLE_SCALE, "f32", batch=3, steps=8, seed=21)
+
+
+def test_decode_production_b64_bf16():
+    """The B=64, H_k=16, H_v=32, d=128 decode workload, three consecutive steps, every sequence checked."""
+    _run_decode_steps(synth.PRODUCTION, "bf16", batch=64, steps=3, seed=2)
+
+
+@pytest.mark.parametrize("dk,dv,hk,hv", [(32, 32, 1, 1), (64, 64, 2, 2), (64, 96, 2, 8), (128, 64, 4, 16),
+                                         (256, 128, 1, 2), (32, 256, 2, 4)])
+def test_decode_head_shapes(dk, dv, hk, hv):
+    _run_decode_steps(synth.Shape(hk, hv, dk, dv, 4), "bf16", batch=5, steps=3, seed=dk + dv + hv)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 8])
+def test_decode_conv_widths(K):
+    _run_decode_steps(synth.Shape(2, 4, 32, 32, K), "f32", batch=2, steps=K + 2, seed=40 + K, conv_kernel=K)
+
+
+def test_decode_without_l2norm():
+    _run_decode_steps(synth.Shape(2, 4, 64, 32, 4), "f32", batch=2, steps=3, seed=77, use_l2=False)
+
+
+def test_decode_batch_zero_is_noop():
+    dev = device()
+    cfg, _ = configs(synth.ORACLE_SCALE, "f32")
+    gb.gdn_forward_decode(cfg, 0, *[torch.empty(16, device=dev)] * 7)

@@ -1,0 +1,168 @@
+"""Prefill over cu_seqlens-packed sequences against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_causal_gb300 import binding as gb
+from gated_deltanet_linear_causal_gb300 import synth
+from gdn_testutil import assert_parity, bits, configs, device, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [gb.GDN_PREFILL_RESIDENT]
+
+
+def _prefill_dev(cfg, x, dev, variant, io):
+    cvt = (lambda a: a) if io == "bf16" else synth.bf16_bits_to_f32
+    cu = x["cu_seqlens"]
+    N, T = len(cu) - 1, int(cu[-1])
+    H, dv = cfg.num_v_heads, cfg.head_v_dim
+    d = dict(cu=to_dev(cu, dev), qkv=to_dev(cvt(x["qkv"]), dev), w=to_dev(cvt(x["conv_weight"]), dev),
+             gate=to_dev(x["gate"], dev), beta=to_dev(x["beta"], dev), conv=to_dev(cvt(x["conv_state"]), dev),
+             S=to_dev(x["ssm_state"], dev), out=torch.full((T, H, dv), float("nan"), device=dev))
+    ws = torch.empty(max(1, gb.gdn_prefill_workspace_size(cfg, N, T, variant)), dtype=torch.uint8, device=dev)
+    gb.gdn_forward_prefill(cfg, N, d["cu"], torch.from_numpy(cu), d["qkv"], d["w"], d["gate"], d["beta"], d["conv"],
+                           d["S"], d["out"], variant, ws)
+    return d
+
+
+def _oracle_prefill(ocfg, x, seq_index=None):
+    return oracle.prefill(ocfg, x["cu_seqlens"], f64(x["qkv"]), f64(x["conv_weight"]), x["gate"], x["beta"],
+                          f64(x["conv_state"]), x["ssm_state"], seq_index)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_oracle_scale_f32(variant):
+    """B=1, L=64, H_k=2, H_v=4, d=32, K=4, fp32 inputs, zero initial states."""
+    dev = device()
+    shape = synth.ORACLE_SCALE
+    cfg, ocfg = configs(shape, "f32")
+    s = synth.oracle_scale(seed=1)
+    x = dict(cu_seqlens=np.array([0, 64], np.int32), qkv=s["qkv"][0], conv_weight=s["conv_weight"],
+             gate=s["gate"][0], beta=s["beta"][0], conv_state=s["conv_state"], ssm_state=s["ssm_state"])
+    d = _prefill_dev(cfg, x, dev, variant, "f32")
+    o_r, c_r, S_r = _oracle_prefill(ocfg, x)
+    torch.cuda.synchronize()
+    assert_parity(f64(d["out"]), o_r, f64(d["S"]), S_r)
+    assert np.array_equal(f64(d["conv"]), c_r)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_prefill_varlen_ragged(variant, io):
+    """Empty sequences, sequences shorter than the conv window, and ragged tails."""
+    dev = device()
+    shape = synth.Shape(2, 4, 32, 64, 4)
+    cfg, ocfg = configs(shape, io)
+    lengths = [0, 1, 2, 3, 17, 40, 0, 5, 130, 1]
+    x = synth.varlen_prefill(seed=31, shape=shape, lengths=lengths)
+    d = _prefill_dev(cfg, x, dev, variant, io)
+    o_r, c_r, S_r = _oracle_prefill(ocfg, x)
+    torch.cuda.synchronize()
+    assert_parity(f64(d["out"]), o_r, f64(d["S"]), S_r)
+    assert np.array_equal(f64(d["conv"]), c_r)
+
+
+@pytest.mark.parametrize("dk,dv,hk,hv,K", [(64, 64, 1, 1, 4), (128, 32, 2, 8, 2), (256, 64, 1, 2, 4),
+                                           (32, 96, 3, 6, 1)])
+def test_prefill_head_shapes(dk, dv, hk, hv, K):
+    dev = device()
+    shape = synth.Shape(hk, hv, dk, dv, K)
+    cfg, ocfg = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=dk + dv, shape=shape, lengths=[37, 3, 64])
+    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    o_r, c_r, S_r = _oracle_prefill(ocfg, x)
+    torch.cuda.synchronize()
+    assert_parity(f64(d["out"]), o_r, f64(d["S"]), S_r)
+    assert np.array_equal(f64(d["conv"]), c_r)
+
+
+def test_prefill_split_bitwise_equals_whole():
+    """Two calls with carried conv and SSM states give the bits of one call."""
+    dev = device()
+    shape = synth.Shape(2, 4, 64, 64, 4)
+    cfg, _ = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=55, shape=shape, lengths=[90])
+    whole = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    cut = 37
+    a = dict(x, cu_seqlens=np.array([0, cut], np.int32), qkv=np.ascontiguousarray(x["qkv"][:, :cut]),
+             gate=x["gate"][:cut], beta=x["beta"][:cut])
+    da = _prefill_dev(cfg, a, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    torch.cuda.synchronize()
+    b = dict(x, cu_seqlens=np.array([0, 90 - cut], np.int32), qkv=np.ascontiguousarray(x["qkv"][:, cut:]),
+             gate=x["gate"][cut:], beta=x["beta"][cut:],
+             conv_state=da["conv"].cpu().view(torch.int16).numpy().view(np.uint16),
+             ssm_state=da["S"].cpu().numpy())
+    db = _prefill_dev(cfg, b, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(torch.cat([da["out"], db["out"]])), bits(whole["out"]))
+    assert np.array_equal(bits(db["S"]), bits(whole["S"]))
+    assert np.array_equal(bits(db["conv"]), bits(whole["conv"]))
+
+
+def _oracle_heads(ocfg, x, n, heads):
+    """Oracle outputs and final states of value heads `heads` of sequence n only
+    (heads are independent: each needs its key head's Q/K channels and its V channels)."""
+    Hk, Hv, dk, dv, K = ocfg.num_k_heads, ocfg.num_v_heads, ocfg.head_k_dim, ocfg.head_v_dim, ocfg.conv_kernel
+    f = Hv // Hk
+    cu = x["cu_seqlens"]
+    a, b = int(cu[n]), int(cu[n + 1])
+    sub = oracle.Cfg(1, 1, dk, dv, K, ocfg.use_qk_l2norm, ocfg.l2norm_eps)
+    res = {}
+    for h in heads:
+        hk = h // f
+        ch = np.r_[hk * dk:(hk + 1) * dk, Hk * dk + hk * dk:Hk * dk + (hk + 1) * dk,
+                   2 * Hk * dk + h * dv:2 * Hk * dk + (h + 1) * dv]
+        r = oracle.forward_sequence(sub, f64(x["qkv"][ch, a:b]), f64(x["conv_weight"][ch]),
+                                    f64(x["conv_state"][n][ch]), x["ssm_state"][n][h:h + 1],
+                                    x["gate"][a:b, h:h + 1], x["beta"][a:b, h:h + 1])
+        res[h] = (r["o"][:, 0], r["S"][0])
+    return res
+
+
+def test_prefill_long_production_sampled_heads():
+    """B=1, L=8192, H_k=16, H_v=32, d=128, slow decay: the whole layer on the GPU;
+    the oracle recomputes value heads 0, 13 and 31 over the full sequence."""
+    dev = device()
+    shape = synth.PRODUCTION
+    cfg, ocfg = configs(shape, "bf16")
+    x = synth.long_prefill(seed=3)
+    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    ref = _oracle_heads(ocfg, x, 0, [0, 13, 31])
+    torch.cuda.synchronize()
+    out, S = f64(d["out"]), f64(d["S"])
+    assert np.isfinite(out).all()
+    for h, (o_r, S_r) in ref.items():
+        assert_parity(out[:, h], o_r, S[0, h], S_r, what=f"head {h}")
+    tail = f64(x["qkv"][:, -3:])
+    assert np.array_equal(f64(d["conv"])[0], tail), "conv state = last K-1 raw inputs"
+
+
+def test_prefill_varlen_production_sampled():
+    """16 sequences with lengths U{256..2048}, random per-sequence states: the oracle
+    recomputes 3 sequences x 3 value heads."""
+    dev = device()
+    shape = synth.PRODUCTION
+    cfg, ocfg = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=4)
+    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    torch.cuda.synchronize()
+    out, S = f64(d["out"]), f64(d["S"])
+    cu = x["cu_seqlens"]
+    for n in (0, 7, 15):
+        for h, (o_r, S_r) in _oracle_heads(ocfg, x, n, [1, 16, 30]).items():
+            assert_parity(out[cu[n]:cu[n + 1], h], o_r, S[n, h], S_r, what=f"seq {n} head {h}")
+        assert np.array_equal(f64(d["conv"])[n], f64(x["qkv"][:, cu[n + 1] - 3:cu[n + 1]]))
+
+
+def test_prefill_empty_is_noop():
+    dev = device()
+    cfg, _ = configs(synth.ORACLE_SCALE, "f32")
+    z = torch.zeros(64, device=dev)
+    conv = torch.zeros(2, cfg.D, 3, device=dev)
+    S = torch.ones(2, 4, 32, 32, device=dev)
+    gb.gdn_forward_prefill(cfg, 2, torch.zeros(3, dtype=torch.int32, device=dev), np.zeros(3, np.int32), z, z, z, z,
+                           conv, S, z, gb.GDN_PREFILL_RESIDENT, None)
+    torch.cuda.synchronize()
+    assert bool((S == 1).all())
