@@ -25,7 +25,8 @@ GDN_BF16, GDN_F32 = 0, 1
 GDN_PREFILL_RESIDENT, GDN_PREFILL_CHUNKED = 0, 1
 
 EXPORTED = ("gdn_conv_state_init", "gdn_forward_decode", "gdn_prefill_workspace_size", "gdn_forward_prefill",
-            "gdn_forward_verify", "gdn_verify_commit", "gdn_status_string", "gdn_last_cuda_error")
+            "gdn_forward_verify", "gdn_verify_commit", "gdn_status_string", "gdn_last_cuda_error",
+            "gdn_device_error")
 
 
 class GdnError(RuntimeError):
@@ -84,6 +85,8 @@ def load(path: str | None = None):
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_last_cuda_error.argtypes = []
         lib.gdn_last_cuda_error.restype = i32
+        lib.gdn_device_error.argtypes = [ctypes.POINTER(i32), i32]
+        lib.gdn_device_error.restype = i32
         for name in ("gdn_conv_state_init", "gdn_forward_decode", "gdn_forward_prefill", "gdn_forward_verify",
                      "gdn_verify_commit"):
             getattr(lib, name).restype = i32
@@ -123,7 +126,7 @@ def _dev(name, t, dtype, numel, optional=False):
         raise ValueError(f"{name}: must be contiguous")
     if t.numel() < numel:
         raise ValueError(f"{name}: {t.numel()} elements, needs {numel}")
-    return t.data_ptr()
+    return t.data_ptr() if t.numel() else None
 
 
 def gdn_conv_state_init(cfg, batch, conv_state, ssm_state, stream=None):
@@ -135,6 +138,8 @@ def gdn_conv_state_init(cfg, batch, conv_state, ssm_state, stream=None):
 
 
 def gdn_forward_decode(cfg, batch, qkv, conv_weight, gate, beta, conv_state, ssm_state, out, stream=None):
+    if batch == 0:
+        return
     D, K, H = cfg.D, cfg.conv_kernel, cfg.num_v_heads
     io = cfg.torch_dtype
     args = [_dev("qkv", qkv, io, batch * D), _dev("conv_weight", conv_weight, io, D * K),
@@ -156,6 +161,8 @@ def gdn_forward_prefill(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_we
     if host.is_cuda or host.numel() < num_seqs + 1:
         raise ValueError("cu_seqlens_host: host int32 tensor of num_seqs+1 entries")
     T = int(host[num_seqs]) if num_seqs > 0 else 0
+    if T == 0:
+        return
     D, K, H = cfg.D, cfg.conv_kernel, cfg.num_v_heads
     io = cfg.torch_dtype
     ws_need = gdn_prefill_workspace_size(cfg, num_seqs, T, variant)
@@ -173,6 +180,8 @@ def gdn_forward_prefill(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_we
 
 def gdn_forward_verify(cfg, batch, L, qkv, conv_weight, gate, beta, conv_state, ssm_state, conv_snap, ssm_snap, out,
                        stream=None):
+    if batch == 0:
+        return
     D, K, H = cfg.D, cfg.conv_kernel, cfg.num_v_heads
     io = cfg.torch_dtype
     S = cfg.num_v_heads * cfg.head_k_dim * cfg.head_v_dim
@@ -187,6 +196,8 @@ def gdn_forward_verify(cfg, batch, L, qkv, conv_weight, gate, beta, conv_state, 
 
 
 def gdn_verify_commit(cfg, batch, L, accepted, conv_snap, ssm_snap, conv_state, ssm_state, status=None, stream=None):
+    if batch == 0:
+        return
     D, K = cfg.D, cfg.conv_kernel
     io = cfg.torch_dtype
     S = cfg.num_v_heads * cfg.head_k_dim * cfg.head_v_dim
@@ -204,3 +215,10 @@ def gdn_status_string(status: int) -> str:
 
 def gdn_last_cuda_error() -> int:
     return int(load().gdn_last_cuda_error())
+
+
+def gdn_device_error(clear=False) -> int:
+    """Synchronous diagnostic: the library's device-side error word (0: none)."""
+    v = ctypes.c_int32(0)
+    _check("gdn_device_error", load().gdn_device_error(ctypes.byref(v), int(bool(clear))))
+    return int(v.value)

@@ -73,6 +73,11 @@ const char* gdn_status_string(gdn_status_t s) {
 
 int32_t gdn_last_cuda_error(void) { return g_last_cuda_error; }
 
+gdn_status_t gdn_device_error(int32_t* value, int32_t clear) {
+    if (!value) return GDN_ERR_NULL;
+    return cuda_status(gdn::stream_error_read(value, clear != 0));
+}
+
 gdn_status_t gdn_conv_state_init(const gdn_config_t* cfg, int32_t batch, void* conv_state, float* ssm_state,
                                  gdn_stream_t stream) {
     gdn::Geom g;
@@ -97,9 +102,17 @@ gdn_status_t gdn_forward_decode(const gdn_config_t* cfg, int32_t batch, const vo
     gdn_status_t st = check_config(cfg, &g);
     if (st != GDN_OK) return st;
     if (batch < 0 || batch > 65535) return GDN_ERR_SHAPE;
-    if (g.dv / 32 * g.f > 16) return GDN_ERR_UNSUPPORTED;  // one cluster per key head
+    {
+        gdn::StepArgs probe{};
+        probe.g = g;
+        probe.B = batch;
+        probe.L = 1;
+        int ns = 0;
+        size_t sm = 0;
+        if (!gdn::stream_step_supported(probe, &ns, &sm) && !gdn::slice_step_supported(g)) return GDN_ERR_UNSUPPORTED;
+    }
     if (batch == 0) return GDN_OK;
-    if (!qkv || !conv_weight || !gate || !beta || !conv_state || !ssm_state || !out) return GDN_ERR_NULL;
+    if (!qkv || !conv_weight || !gate || !beta || (!conv_state && g.K > 1) || !ssm_state || !out) return GDN_ERR_NULL;
     const size_t eb = elem_bytes(cfg);
     if (!aligned(qkv, 16) || !aligned(ssm_state, 16) || !aligned(out, 16) || !aligned(conv_weight, eb) ||
         !aligned(conv_state, eb) || !aligned(gate, 4) || !aligned(beta, 4))
@@ -129,7 +142,8 @@ gdn_status_t gdn_forward_verify(const gdn_config_t* cfg, int32_t batch, int32_t 
     if (st != GDN_OK) return st;
     if (batch < 0 || batch > 65535 || L < 1 || L > 16) return GDN_ERR_SHAPE;
     if (batch == 0) return GDN_OK;
-    if (!qkv || !conv_weight || !gate || !beta || !conv_state || !ssm_state || !conv_snap || !ssm_snap || !out)
+    if (!qkv || !conv_weight || !gate || !beta || (g.K > 1 && (!conv_state || !conv_snap)) || !ssm_state ||
+        !ssm_snap || !out)
         return GDN_ERR_NULL;
     const size_t eb = elem_bytes(cfg);
     if (!aligned(qkv, 16) || !aligned(ssm_state, 16) || !aligned(ssm_snap, 16) || !aligned(out, 16) ||
@@ -160,7 +174,7 @@ gdn_status_t gdn_verify_commit(const gdn_config_t* cfg, int32_t batch, int32_t L
     if (st != GDN_OK) return st;
     if (batch < 0 || batch > 65535 || L < 1 || L > 16) return GDN_ERR_SHAPE;
     if (batch == 0) return GDN_OK;
-    if (!accepted || !conv_snap || !ssm_snap || !conv_state || !ssm_state) return GDN_ERR_NULL;
+    if (!accepted || (g.K > 1 && (!conv_snap || !conv_state)) || !ssm_snap || !ssm_state) return GDN_ERR_NULL;
     const size_t eb = elem_bytes(cfg);
     if (!aligned(accepted, 4) || !aligned(ssm_snap, 16) || !aligned(ssm_state, 16) || !aligned(conv_snap, eb) ||
         !aligned(conv_state, eb) || (status && !aligned(status, 4)))
@@ -208,7 +222,7 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, cons
     const int64_t T = cu_seqlens_host[num_seqs];
     if (T == 0) return GDN_OK;
     if (variant == GDN_PREFILL_CHUNKED) return GDN_ERR_UNSUPPORTED;
-    if (!qkv || !conv_weight || !gate || !beta || !conv_state || !ssm_state || !out) return GDN_ERR_NULL;
+    if (!qkv || !conv_weight || !gate || !beta || (!conv_state && g.K > 1) || !ssm_state || !out) return GDN_ERR_NULL;
     const size_t eb = elem_bytes(cfg);
     if (!aligned(cu_seqlens, 4) || !aligned(qkv, 16) || !aligned(ssm_state, 16) || !aligned(out, 16) ||
         !aligned(conv_weight, eb) || !aligned(conv_state, eb) || !aligned(gate, 4) || !aligned(beta, 4))

@@ -31,7 +31,14 @@ struct StepArgs {
     float* S_out;         // decode: S_in;    verify: [B, L, Hv, dk, dv]
     float* out;           // [B, L, Hv, dv]
 };
+// Decode / verify.  launch_step picks the persistent TMA-fed kernel
+// (gdn_stream.cu) when stream_step_supported() accepts the shape, else the
+// cluster-per-key-head slice kernel (gdn_step.cu).
 cudaError_t launch_step(const StepArgs& a, bool in_place, cudaStream_t stream);
+bool stream_step_supported(const StepArgs& a, int* nstage, size_t* smem_bytes);
+cudaError_t launch_stream_step(const StepArgs& a, bool in_place, cudaStream_t stream);
+bool slice_step_supported(const Geom& g);
+cudaError_t stream_error_read(int32_t* value, bool clear);
 
 struct CommitArgs {
     int B, L;

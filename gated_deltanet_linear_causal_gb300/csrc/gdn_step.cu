@@ -252,7 +252,12 @@ __global__ void zero_kernel(unsigned char* p, size_t head, size_t n16, size_t ta
 
 }  // namespace
 
+bool slice_step_supported(const Geom& g) { return (g.dv / kSliceCols) * g.f <= 16; }
+
 cudaError_t launch_step(const StepArgs& a, bool in_place, cudaStream_t stream) {
+    int ns = 0;
+    size_t smem = 0;
+    if (stream_step_supported(a, &ns, &smem)) return launch_stream_step(a, in_place, stream);
     return in_place ? dispatch_step<true>(a, stream) : dispatch_step<false>(a, stream);
 }
 

@@ -32,8 +32,11 @@
  *     conv states need their element alignment.
  *   - Supported shapes: head_k_dim in {32, 64, 128, 256}; head_v_dim a
  *     multiple of 32 up to 512; num_v_heads a multiple of num_k_heads; conv
- *     kernel 1..8; ((head_v_dim/32) * (num_v_heads/num_k_heads)) <= 16 for
- *     decode.  Others return GDN_ERR_UNSUPPORTED.
+ *     kernel 1..8; for decode either head_k_dim in {64, 128} with head_v_dim
+ *     a multiple of 128, or (head_v_dim/32) * (num_v_heads/num_k_heads) <= 16.
+ *     Others return GDN_ERR_UNSUPPORTED.
+ *   - With conv_kernel K = 1 the conv state is empty and its pointers may be
+ *     NULL.
  *   - The output is fp32, token-major [.., L, Hv, dv]: the layout the next
  *     step of the layer (gated RMSNorm over value_dim, section 2) reads.
  */
@@ -58,7 +61,7 @@ typedef enum {
     GDN_ERR_DTYPE = 4,          /* io_dtype is not a gdn_dtype_t */
     GDN_ERR_SEQLENS = 5,        /* cu_seqlens does not start at 0 or is not non-decreasing */
     GDN_ERR_CUDA = 6,           /* a CUDA launch failed; see gdn_last_cuda_error() */
-    GDN_ERR_DEVICE_TIMEOUT = 7, /* reserved: a bounded device-side wait gave up */
+    GDN_ERR_DEVICE_TIMEOUT = 7, /* a bounded device-side wait gave up (see gdn_device_error) */
     GDN_ERR_UNSUPPORTED = 8,    /* valid but not built (head size, GQA ratio, variant) */
     GDN_ERR_WORKSPACE = 9,      /* workspace missing or smaller than gdn_prefill_workspace_size() */
     GDN_ERR_RANGE = 10          /* device-side: an accepted length outside [0, L] */
@@ -186,6 +189,15 @@ const char *gdn_status_string(gdn_status_t status);
 
 /* CUDA error code (cudaError_t) behind the calling thread's last GDN_ERR_CUDA. */
 int32_t gdn_last_cuda_error(void);
+
+/*
+ * Diagnostic, synchronous: read (and with clear != 0, reset) the library's
+ * device-side error word of the current device.  Kernels never wait without a
+ * bound: a wait on an asynchronous copy that gives up sets the word to
+ * GDN_ERR_DEVICE_TIMEOUT and the kernel returns early, leaving that call's
+ * outputs incomplete.  0 means no such event since the last reset.
+ */
+gdn_status_t gdn_device_error(int32_t *value, int32_t clear);
 
 #ifdef __cplusplus
 }

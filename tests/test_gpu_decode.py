@@ -44,7 +44,9 @@ def test_decode_production_b64_bf16():
 
 
 @pytest.mark.parametrize("dk,dv,hk,hv", [(32, 32, 1, 1), (64, 64, 2, 2), (64, 96, 2, 8), (128, 64, 4, 16),
-                                         (256, 128, 1, 2), (32, 256, 2, 4)])
+                                         (256, 128, 1, 2), (32, 256, 2, 4),
+                                         # shapes of the persistent bulk-copy kernel (dk 64/128, dv % 128 == 0)
+                                         (64, 128, 2, 4), (128, 256, 2, 4), (128, 128, 1, 4), (64, 384, 3, 3)])
 def test_decode_head_shapes(dk, dv, hk, hv):
     _run_decode_steps(synth.Shape(hk, hv, dk, dv, 4), "bf16", batch=5, steps=3, seed=dk + dv + hv)
 

@@ -14,7 +14,7 @@ VARIANTS = [gb.GDN_PREFILL_RESIDENT]
 
 
 def _prefill_dev(cfg, x, dev, variant, io):
-    cvt = (lambda a: a) if io == "bf16" else synth.bf16_bits_to_f32
+    cvt = (lambda a: a) if io == "bf16" else (lambda a: synth.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a)
     cu = x["cu_seqlens"]
     N, T = len(cu) - 1, int(cu[-1])
     H, dv = cfg.num_v_heads, cfg.head_v_dim

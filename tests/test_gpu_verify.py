@@ -58,11 +58,12 @@ def test_verify_production_b32_l4_and_commit():
     assert np.array_equal(f64(x["conv"]), conv_r)
 
 
-@pytest.mark.parametrize("io,dk", [("bf16", 128), ("f32", 32), ("bf16", 64), ("f32", 256)])
-def test_verify_snapshot_bitwise_equals_decode(io, dk):
+@pytest.mark.parametrize("io,dk,dv", [("bf16", 128, 64), ("f32", 32, 64), ("bf16", 64, 64), ("f32", 256, 64),
+                                      ("bf16", 128, 128), ("f32", 64, 128), ("bf16", 128, 256)])
+def test_verify_snapshot_bitwise_equals_decode(io, dk, dv):
     """Snapshot t equals, bit for bit, the states t+1 decode calls leave (the verify
     block and single steps run the same per-token arithmetic)."""
-    shape = synth.Shape(2, 4, dk, 64, 4)
+    shape = synth.Shape(2, 4, dk, dv, 4)
     L, batch = 5, 3
     cfg, ocfg, v, x, csnap, ssnap, out = _verify(shape, io, batch, L, seed=dk)
     dev = x["S"].device
