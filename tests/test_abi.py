@@ -59,7 +59,9 @@ def test_config_validation(lib):
     assert _decode(lib, _cfg(conv_kernel=9)) == 8
     assert _decode(lib, _cfg(conv_kernel=0)) == 2
     assert _decode(lib, _cfg(num_k_heads=0)) == 2
-    assert _decode(lib, _cfg(head_v_dim=512, num_v_heads=64)) == 8  # cluster of 16*4 CTAs too large
+    # neither decode kernel: dk=32 is outside the bulk-copy kernel, and the slice kernel's
+    # cluster would need (512/32) * 4 = 64 CTAs
+    assert _decode(lib, _cfg(head_k_dim=32, head_v_dim=512, num_v_heads=64)) == 8
     assert lib.gdn_forward_decode(None, 1, *[FAKE] * 7, None) == 1
     assert binding.gdn_status_string(8).startswith("shape or variant")
 
