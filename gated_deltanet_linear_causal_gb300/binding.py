@@ -222,3 +222,30 @@ def gdn_device_error(clear=False) -> int:
     v = ctypes.c_int32(0)
     _check("gdn_device_error", load().gdn_device_error(ctypes.byref(v), int(bool(clear))))
     return int(v.value)
+
+
+def gdn_forward_prefill_noalloc(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_weight, gate, beta, conv_state,
+                                ssm_state, out, stream=None):
+    """Resident prefill with the library's fixed workspace (no allocation by anyone):
+    for callers that cannot call cudaMalloc.  Same arguments as gdn_forward_prefill
+    minus variant and workspace; T * D * 4 must fit GDN_NOALLOC_SCRATCH_BYTES."""
+    lib = load()
+    if not hasattr(lib, "_noalloc_typed"):
+        vp = ctypes.c_void_p
+        lib.gdn_forward_prefill_noalloc.argtypes = [ctypes.POINTER(gdn_config_t), ctypes.c_int32] + [vp] * 10
+        lib.gdn_forward_prefill_noalloc.restype = ctypes.c_int32
+        lib._noalloc_typed = True
+    host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    if host.is_cuda or host.numel() < num_seqs + 1:
+        raise ValueError("cu_seqlens_host: host int32 tensor of num_seqs+1 entries")
+    T = int(host[num_seqs]) if num_seqs > 0 else 0
+    D, K, H = cfg.D, cfg.conv_kernel, cfg.num_v_heads
+    io = cfg.torch_dtype
+    args = [_dev("cu_seqlens", cu_seqlens, torch.int32, num_seqs + 1), host.data_ptr(),
+            _dev("qkv", qkv, io, D * T), _dev("conv_weight", conv_weight, io, D * K),
+            _dev("gate", gate, torch.float32, T * H), _dev("beta", beta, torch.float32, T * H),
+            _dev("conv_state", conv_state, io, num_seqs * D * (K - 1)),
+            _dev("ssm_state", ssm_state, torch.float32, num_seqs * H * cfg.head_k_dim * cfg.head_v_dim),
+            _dev("out", out, torch.float32, T * H * cfg.head_v_dim)]
+    _check("gdn_forward_prefill_noalloc",
+           lib.gdn_forward_prefill_noalloc(ctypes.byref(cfg), num_seqs, *args, _stream(stream)))

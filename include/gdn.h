@@ -150,6 +150,39 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t *cfg, int32_t num_seqs,
                                  size_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * Prefill for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is a deployment convenience, not part of the layer.)
+ *
+ * gdn_forward_prefill needs a workspace from the caller.  A caller that runs
+ * inside a host framework owning all device memory through its own pool, or a
+ * serving loop that may not call cudaMalloc (which can synchronise the device),
+ * has no way to provide one.  This entry point runs the same resident prefill
+ * (GDN_PREFILL_RESIDENT) with its workspace in a fixed array of
+ * GDN_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads
+ * the library holds that memory until the process exits.  It calls no
+ * allocator.  Arguments, layouts and results are those of gdn_forward_prefill.
+ *
+ *   - Limit: the workspace is T * D * 4 bytes (T = cu_seqlens_host[num_seqs]),
+ *     so T * D * 4 <= GDN_NOALLOC_SCRATCH_BYTES (at D = 8192: T <= 512).
+ *     Larger calls return GDN_ERR_WORKSPACE and launch nothing.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.  GDN_ERR_CUDA if the lookup
+ *     fails.
+ *   - Sharing: every call on a device uses the same array, which keeps the last
+ *     call's contents.  Calls that can overlap on the GPU (different streams
+ *     without ordering between them) race on it; order them.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (16u << 20)
+gdn_status_t gdn_forward_prefill_noalloc(const gdn_config_t *cfg, int32_t num_seqs,
+                                         const int32_t *cu_seqlens,
+                                         const int32_t *cu_seqlens_host,
+                                         const void *qkv, const void *conv_weight,
+                                         const float *gate, const float *beta,
+                                         void *conv_state, float *ssm_state, float *out,
+                                         gdn_stream_t stream);
+
+/*
  * MTP verify: run L draft tokens per sequence from the live states, which are
  * only read, and write the state after every token so that a rejected suffix
  * can be dropped exactly (the verify forward of an MTP round processes its
