@@ -158,15 +158,22 @@ def verify_bytes(shape, B, L):
             2 * B * L * shape.num_v_heads * 4 + shape.D * shape.conv_kernel * 2)
 
 
-def run_decode(args, dev, dist, rank, world):
+def decode_inputs(args, rank):
+    from gated_deltanet_linear_causal_gb300 import synth
+    shape = synth.PRODUCTION
+    st = synth.decode_state(2 + 1000 * rank, B_DECODE, shape)
+    n_in = min(N_INPUT_STEPS, max(args.steps, 1) + args.warmup)
+    steps = [synth.decode_step(2 + 1000 * rank, s, B_DECODE, shape) for s in range(n_in)]
+    return st, steps
+
+
+def run_decode(args, dev, dist, rank, world, st, steps):
     import numpy as np
     import torch
     from gated_deltanet_linear_causal_gb300 import binding as gb, synth
     shape = synth.PRODUCTION
     cfg = gb.make_config(16, 32, 128, 128, 4, True, 1e-6, "bf16")
-    st = synth.decode_state(2 + 1000 * rank, B_DECODE, shape)
-    n_in = min(N_INPUT_STEPS, max(args.steps, 1) + args.warmup)
-    steps = [synth.decode_step(2 + 1000 * rank, s, B_DECODE, shape) for s in range(n_in)]
+    n_in = len(steps)
     qkv = torch.stack([_to_dev(s["qkv"], dev) for s in steps])
     gate = torch.stack([_to_dev(s["gate"], dev) for s in steps])
     beta = torch.stack([_to_dev(s["beta"], dev) for s in steps])
@@ -185,17 +192,11 @@ def run_decode(args, dev, dist, rank, world):
 
     for i in range(args.warmup):
         step(i)
-    # untimed soak (~1 s) so the clock sampler sees the GPU under this load
-    clocks = ClockSampler(dev.index)
-    clocks.start()
+    # untimed soak (at most args.soak launches, ~40 ms) so clocks settle under this load
     torch.cuda.synchronize()
-    t_end = time.perf_counter() + 1.0
-    i = 0
-    while time.perf_counter() < t_end:
-        for _ in range(64):
-            step(i)
-            i += 1
-        torch.cuda.synchronize()
+    for i in range(args.soak):
+        step(i)
+    torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -207,7 +208,6 @@ def run_decode(args, dev, dist, rank, world):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     if dist:
         t = torch.tensor([ms], device=dev)
@@ -217,6 +217,9 @@ def run_decode(args, dev, dist, rank, world):
     value = tokens / (ms / 1e3)
     launch_us = ms * 1e3 / args.steps
 
+    if args.no_e2e:
+        return dict(ms=ms, value=value, launch_us=launch_us, bytes=per_step, rotation=R, e2e=None,
+                     inputs=dict(steps=steps, state=st))
     # end to end through the public binding: pinned host inputs in, output back to pinned host
     h_qkv = [_pinned(s["qkv"]) for s in steps]
     h_gate = [_pinned(s["gate"]) for s in steps]
@@ -249,8 +252,8 @@ def run_decode(args, dev, dist, rank, world):
         ms_e2e = float(t.item())
     h2d = h_qkv[0].numel() * 2 + h_gate[0].numel() * 4 + h_beta[0].numel() * 4
     d2h = h_out.numel() * 4
-    return dict(ms=ms, value=value, launch_us=launch_us, bytes=per_step, rotation=R, clocks=clk,
-                e2e=dict(value=tokens / (ms_e2e / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
+    return dict(ms=ms, value=value, launch_us=launch_us, bytes=per_step, rotation=R,
+                e2e=None if args.no_e2e else dict(value=tokens / (ms_e2e / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h), inputs=dict(steps=steps, state=st))
 
 
@@ -369,6 +372,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-secondary", action="store_true", help="headline decode only")
+    ap.add_argument("--soak", type=int, default=500, help="untimed decode launches before the timed region")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -383,14 +388,40 @@ def main():
     from gated_deltanet_linear_causal_gb300 import binding as gb, synth
     gb.load()
     peaks = _peaks()
-    dec = run_decode(args, dev, dist, rank, world)
+    secondary = world == 1 and not args.no_secondary
+    st, steps = decode_inputs(args, rank)
+    if secondary:  # host-side input generation happens before the GPU-timed phases
+        x_long, x_var, x_ver = synth.long_prefill(seed=3), synth.varlen_prefill(seed=4), synth.verify_block(seed=5)
+    clocks = ClockSampler(dev.index)  # samples across the GPU phases of this run
+    clocks.start()
+    dec = run_decode(args, dev, dist, rank, world, st, steps)
+    sec = {}
+    if secondary and rank == 0:
+        shape = synth.PRODUCTION
+        med, times = run_prefill(dev, x_long, gb.GDN_PREFILL_RESIDENT)
+        nb = prefill_bytes(shape, x_long["cu_seqlens"], False)
+        sec["prefill_L8192"] = {"variant": "resident", "tokens_per_s": round(8192 / (med / 1e3), 1),
+                                "ms": round(med, 4), "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
+        med, _ = run_prefill(dev, x_var, gb.GDN_PREFILL_RESIDENT)
+        T = int(x_var["cu_seqlens"][-1])
+        nb = prefill_bytes(shape, x_var["cu_seqlens"], True)
+        sec["prefill_varlen16"] = {"variant": "resident", "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
+                                   "ms": round(med, 4),
+                                   "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                   "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
+        mv, mc = run_verify(dev, x_ver)
+        nb = verify_bytes(shape, 32, 4)
+        sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4),
+                                "roofline_frac": round(nb / (mv / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": nb, "commit_ms": round(mc, 4), "cold_l2": True}
+    clk = clocks.stop()
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
-    shape = synth.PRODUCTION
     achieved = dec["bytes"] / (dec["launch_us"] * 1e-6) / 1e9
-    sources = ["gdn_step.cu", "gdn_common.cuh"]
+    sources = ["gdn_stream.cu", "gdn_common.cuh", "gdn_tma.cuh"]
     line = {
         "metric": METRIC, "value": round(dec["value"], 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms"] / args.steps, 5),
@@ -402,38 +433,15 @@ def main():
                                          f"{dec['bytes'] / 1e6:.1f} MB per step"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("decode_b64", sources),
-                     "kernel": "step_kernel<bf16,128,in_place>", "algorithmic_bytes_per_launch": dec["bytes"],
+                     "kernel": "stream_kernel<bf16,128,in_place>", "algorithmic_bytes_per_launch": dec["bytes"],
                      "launch_us": round(dec["launch_us"], 2), "peak_source": peaks["source"]},
-        "e2e": dec["e2e"], "gpu_launches": args.steps, "clocks": dec["clocks"],
+        "e2e": dec["e2e"], "gpu_launches": args.steps, "clocks": clk,
     }
-    if world == 1:
+    if world == 1 and args.cpu_budget > 0:
         v, sample = oracle_decode_rate(dec["inputs"]["steps"], dec["inputs"]["state"], args.cpu_budget, args.steps)
         line["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": sample}
-    if world == 1 and not args.no_secondary:
-        sec = {}
-        x = synth.long_prefill(seed=3)
-        med, times = run_prefill(dev, x, gb.GDN_PREFILL_RESIDENT)
-        nb = prefill_bytes(shape, x["cu_seqlens"], False)
-        sec["prefill_L8192"] = {"variant": "resident", "tokens_per_s": round(8192 / (med / 1e3), 1),
-                                "ms": round(med, 4), "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
-        del x
-        x = synth.varlen_prefill(seed=4)
-        med, _ = run_prefill(dev, x, gb.GDN_PREFILL_RESIDENT)
-        T = int(x["cu_seqlens"][-1])
-        nb = prefill_bytes(shape, x["cu_seqlens"], True)
-        sec["prefill_varlen16"] = {"variant": "resident", "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
-                                   "ms": round(med, 4),
-                                   "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                   "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
-        del x
-        x = synth.verify_block(seed=5)
-        mv, mc = run_verify(dev, x)
-        nb = verify_bytes(shape, 32, 4)
-        sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4),
-                                "roofline_frac": round(nb / (mv / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                "algorithmic_bytes": nb, "commit_ms": round(mc, 4), "cold_l2": True}
+    if sec:
         line["secondary"] = sec
     print(json.dumps(line), flush=True)
     if dist:
