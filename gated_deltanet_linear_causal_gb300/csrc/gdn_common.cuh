@@ -87,13 +87,15 @@ struct ConvWindow {
         for (int j = 0; j < kMaxConv; ++j) acc = fmaf(w[j], x[j], acc);
         return silu(acc);
     }
-    // Entry i (oldest first) of the K-1 sample conv state after the last push.
-    __device__ __forceinline__ T state(int i, int K) const {
-        T r = raw[0];
+    // Write the K-1 sample conv state after the last push (oldest first) to dst.
+    // Loop bounds and register indices are compile-time: the window stays in
+    // registers.
+    __device__ __forceinline__ void store_state(T* dst, int K) const {
 #pragma unroll
-        for (int j = 0; j < kMaxConv; ++j)
-            if (j == kMaxConv + 1 - K + i) r = raw[j];
-        return r;
+        for (int j = 0; j < kMaxConv; ++j) {
+            const int e = j - (kMaxConv + 1 - K);
+            if (e >= 0) dst[e] = raw[j];
+        }
     }
 };
 

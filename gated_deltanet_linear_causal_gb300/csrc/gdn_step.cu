@@ -66,13 +66,10 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const StepArgs a) {
             const float y = win.push(x[t]);
             if (ch < 2 * DK) qk_s[t * 2 * DK + ch] = y;
             else v_s[t * kSliceCols + (ch - 2 * DK)] = y;
-            if (!IN_PLACE && (ch >= 2 * DK || owns_qk)) {
-                T* snap = static_cast<T*>(a.conv_out) + (((size_t)b * L + t) * g.D + c) * (g.K - 1);
-                for (int i = 0; i < g.K - 1; ++i) snap[i] = win.state(i, g.K);
-            }
+            if (!IN_PLACE && (ch >= 2 * DK || owns_qk))
+                win.store_state(static_cast<T*>(a.conv_out) + (((size_t)b * L + t) * g.D + c) * (g.K - 1), g.K);
         }
-        if (IN_PLACE)
-            for (int i = 0; i < g.K - 1; ++i) cs_new[ch * (g.K - 1) + i] = win.state(i, g.K);
+        if (IN_PLACE) win.store_state(cs_new + ch * (g.K - 1), g.K);
     }
     __syncthreads();
     if (IN_PLACE) cluster_arrive_release();  // this CTA is done reading the old conv state

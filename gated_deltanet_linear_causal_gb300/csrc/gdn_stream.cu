@@ -1,23 +1,27 @@
 // gdn_stream.cu -- decode and MTP verify as one persistent, TMA-fed kernel.
 //
 // Work item = (sequence b, key head hk): the f = Hv/Hk value heads that share
-// key head hk (reverse GQA, MNN "Qwen3.5" page, section 1.3).  One CTA per SM
-// walks its items; for each it
-//   1. convolves + SiLUs the 2*dk Q/K channels of hk and the f*dv V channels of
-//      its value heads from the carried conv state (section 1.2 Step 1, section
-//      1.4), L2-normalises q and k and scales q (Steps 2-4), and rewrites the
-//      conv state in place (decode) or writes its per-token snapshots (verify);
-//      because an item owns all channels it reads, no other CTA touches them;
-//   2. streams the item's state tiles (dk rows x 128 columns of one value head)
-//      through a ring of shared-memory stages filled by bulk asynchronous copies
-//      (cp.async.bulk + mbarrier), nstage tiles ahead of the compute;
-//   3. runs the gated delta rule (section 1.2 Step 5) on each tile held in
-//      registers, one token at a time, and stores the new state (decode, in
-//      place) or every per-token snapshot (verify) straight from registers.
+// key head hk (reverse GQA, MNN "Qwen3.5" page, section 1.3).  Owning an item
+// means owning every channel it reads, so the in-place conv-state rewrite has a
+// single reader/writer and needs no cross-CTA synchronisation.  One CTA per SM
+// walks its items with three warp-specialised roles:
+//   producer (1 warp)  keeps a ring of shared-memory stages nstage tiles ahead:
+//                      each tile (dk rows x 128 columns of one value head's fp32
+//                      state) arrives by bulk asynchronous copy (cp.async.bulk,
+//                      completing an mbarrier);
+//   prologue (4 warps) runs steps 1-4 of section 1.2 for the next item into a
+//                      double buffer: conv + SiLU of the 2*dk Q/K channels and
+//                      f*dv V channels from the carried conv state (section 1.4),
+//                      which it rewrites in place (decode) or snapshots per token
+//                      (verify), then the L2 norms and the 1/sqrt(dk) scale;
+//   compute (8 warps)  runs Step 5, the gated delta rule, on each tile held in
+//                      registers, one token at a time, and stores the new state
+//                      (decode, in place) or every per-token snapshot (verify)
+//                      straight from registers.
 // Every byte of state is read from HBM once and written once per token written.
-// Thread (warp w, lane l) of the 8-warp CTA holds columns 4l..4l+3 of rows
-// w + 8m; the reductions over dk go through shared memory in a fixed order, so
-// decode and verify produce identical bits for identical inputs.
+// Compute thread (warp w, lane l) holds columns 4l..4l+3 of rows w + 8m; the
+// reductions over dk go through shared memory in a fixed order, so decode and
+// verify produce identical bits for identical inputs.  Every wait is bounded.
 #include <algorithm>
 
 #include "gdn_common.cuh"
@@ -30,16 +34,22 @@ static __device__ int32_t g_stream_error;  // set to GDN_ERR_DEVICE_TIMEOUT (7) 
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+// Roles of the 13 warps of a CTA.
+constexpr int kComputeWarps = 8;                                // stream state tiles
+constexpr int kPrologWarps = 4;                                 // steps 1-4 of the next item
+constexpr int kProducerWarp = kComputeWarps + kPrologWarps;     // bulk copies into the ring
+constexpr int kCompute = kComputeWarps * 32;
+constexpr int kProlog = kPrologWarps * 32;
+constexpr int kThreads = (kComputeWarps + kPrologWarps + 1) * 32;
+constexpr int kBarCompute = 1, kBarProlog = 2;                  // named barrier ids
 constexpr int kTileCols = 128;
 
 template <int DK>
 struct Tile {
-    static constexpr int RPT = DK / kWarps;  // rows per thread
+    static constexpr int RPT = DK / kComputeWarps;  // rows per thread
     float4 s[RPT];
 
-    __device__ __forceinline__ static int row(int m) { return (threadIdx.x >> 5) + kWarps * m; }
+    __device__ __forceinline__ static int row(int m) { return (threadIdx.x >> 5) + kComputeWarps * m; }
     __device__ __forceinline__ static int col4() { return 4 * (threadIdx.x & 31); }
 
     __device__ __forceinline__ void load_smem(const float* stage) {
@@ -54,7 +64,7 @@ struct Tile {
     // One token of the gated delta rule on the tile (same algebra as
     // StateSlice::step): a = (alpha S)^T k, delta = beta (v - a),
     // S' = alpha S + k delta^T, o = alpha S^T q + delta (k.q).
-    // red: [kWarps][256] shared floats, not in use by any thread.
+    // red: [kComputeWarps][256] shared floats that no compute thread is reading.
     __device__ __forceinline__ float4 step(const float* k, const float* q, float4 v4, float alpha, float beta,
                                            float kq, float* red) {
         float a[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -71,10 +81,10 @@ struct Tile {
         const int warp = threadIdx.x >> 5;
         *reinterpret_cast<float4*>(red + warp * 256 + col4()) = make_float4(a[0], a[1], a[2], a[3]);
         *reinterpret_cast<float4*>(red + warp * 256 + 128 + col4()) = make_float4(c[0], c[1], c[2], c[3]);
-        __syncthreads();
+        named_sync(kBarCompute, kCompute);
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f), C = A;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < kComputeWarps; ++w) {
             const float4 ra = *reinterpret_cast<const float4*>(red + w * 256 + col4());
             const float4 rc = *reinterpret_cast<const float4*>(red + w * 256 + 128 + col4());
             A.x += ra.x; A.y += ra.y; A.z += ra.z; A.w += ra.w;
@@ -94,189 +104,241 @@ struct Tile {
     }
 };
 
-struct Smem {
-    float* stage;  // [nstage][DK * 128]
-    float* qk;     // [L][2*DK]  q then k
-    float* v;      // [L][f*dv]
-    float* coef;   // [kMaxVerify][3]  q factor, k factor, k.q
-    float* nred;   // [kWarps][3*kMaxVerify]
-    float* red;    // [2][kWarps][256]
-    uint64_t* full;  // [nstage]
+// Shared-memory carve-up (dynamic part).
+struct Layout {
+    size_t stage, qk, v, coef, nred, red, bars, total;
+    __host__ __device__ Layout(int DK, int nstage, int L, int f, int dv) {
+        size_t o = 0;
+        stage = o; o += (size_t)nstage * DK * kTileCols * 4;
+        qk = o;    o += (size_t)2 * L * 2 * DK * 4;          // double-buffered by item
+        v = o;     o += (size_t)2 * L * f * dv * 4;
+        coef = o;  o += (size_t)2 * 3 * kMaxVerify * 4;
+        nred = o;  o += (size_t)kPrologWarps * 3 * kMaxVerify * 4;
+        red = o;   o += (size_t)2 * kComputeWarps * 256 * 4;
+        bars = o;  o += (size_t)(2 * nstage + 4) * 8;         // full[ns], empty[ns], qfull[2], qempty[2]
+        total = o;
+    }
 };
 
-__host__ __device__ inline size_t smem_floats(int DK, int nstage, int L, int f, int dv) {
-    return (size_t)nstage * DK * kTileCols + (size_t)L * 2 * DK + (size_t)L * f * dv + 3 * kMaxVerify +
-           kWarps * 3 * kMaxVerify + 2 * kWarps * 256;
+// Geometry of one item's tile r.
+struct TileRef {
+    int b, hk, h, hl, col0;
+};
+__device__ __forceinline__ TileRef tile_ref(const Geom& g, int item, int r) {
+    const int nsl = g.dv / kTileCols;
+    TileRef t;
+    t.b = item / g.Hk;
+    t.hk = item % g.Hk;
+    t.hl = r / nsl;
+    t.h = t.hk * g.f + t.hl;
+    t.col0 = (r % nsl) * kTileCols;
+    return t;
 }
 
 template <typename T, int DK, bool IN_PLACE>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, const int nstage) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ int s_abort;
+    __shared__ int s_abort;    // any role gave up: the others stop waiting
+    __shared__ int s_cabort;   // compute group's own flag (uniform decisions)
+    __shared__ int s_pabort;   // prologue group's own flag
     const Geom& g = a.g;
     const int L = a.L;
     constexpr int TILE = DK * kTileCols;
-    const int nsl = g.dv / kTileCols;  // column tiles per value head
-    const int tpi = g.f * nsl;         // tiles per item
+    const int tpi = g.f * (g.dv / kTileCols);  // tiles per item
     const int nitems = a.B * g.Hk;
     const int my_items = (nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int ntiles = my_items * tpi;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    Smem sm;
-    sm.stage = reinterpret_cast<float*>(smem_raw);
-    sm.qk = sm.stage + (size_t)nstage * TILE;
-    sm.v = sm.qk + L * 2 * DK;
-    sm.coef = sm.v + L * g.f * g.dv;
-    sm.nred = sm.coef + 3 * kMaxVerify;
-    sm.red = sm.nred + kWarps * 3 * kMaxVerify;
-    sm.full = reinterpret_cast<uint64_t*>(sm.red + 2 * kWarps * 256);
-
-    const T* qkv = static_cast<const T*>(a.qkv);
-    const T* w = static_cast<const T*>(a.w);
-    const T* cin = static_cast<const T*>(a.conv_in);
-    T* cout = static_cast<T*>(a.conv_out);
-
-    // Issue the bulk copies of tile j (warp 0 only).
-    auto issue = [&](int j) {
-        const int item = (int)blockIdx.x + (j / tpi) * (int)gridDim.x;
-        const int r = j % tpi;
-        const int b = item / g.Hk, hk = item % g.Hk;
-        const int h = hk * g.f + r / nsl, col0 = (r % nsl) * kTileCols;
-        const float* src = a.S_in + ((size_t)(b * g.Hv + h) * DK) * g.dv + col0;
-        float* dst = sm.stage + (size_t)(j % nstage) * TILE;
-        uint64_t* bar = sm.full + (j % nstage);
-        if (nsl == 1) {
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar, TILE * 4);
-                bulk_g2s(dst, src, TILE * 4, bar);
-            }
-        } else {
-            if (lane == 0) mbar_arrive_expect_tx(bar, TILE * 4);
-            __syncwarp();
-            for (int row = lane; row < DK; row += 32)
-                bulk_g2s(dst + row * kTileCols, src + (size_t)row * g.dv, kTileCols * 4, bar);
-        }
-    };
+    const Layout lay(DK, nstage, L, g.f, g.dv);
+    float* stage = reinterpret_cast<float*>(smem_raw + lay.stage);
+    float* qk_buf = reinterpret_cast<float*>(smem_raw + lay.qk);
+    float* v_buf = reinterpret_cast<float*>(smem_raw + lay.v);
+    float* coef_buf = reinterpret_cast<float*>(smem_raw + lay.coef);
+    float* nred = reinterpret_cast<float*>(smem_raw + lay.nred);
+    float* red = reinterpret_cast<float*>(smem_raw + lay.red);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + lay.bars);
+    uint64_t* empty = full + nstage;
+    uint64_t* qfull = empty + nstage;
+    uint64_t* qempty = qfull + 2;
 
     if (tid == 0) {
-        for (int s = 0; s < nstage; ++s) mbar_init(sm.full + s, 1);
+        for (int s = 0; s < nstage; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kComputeWarps);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(qfull + s, 1);
+            mbar_init(qempty + s, kComputeWarps);
+        }
         fence_mbar_init();
         s_abort = 0;
+        s_cabort = 0;
+        s_pabort = 0;
     }
     __syncthreads();
-    if (warp == 0)
-        for (int j = 0; j < min(nstage, ntiles); ++j) issue(j);
 
-    for (int i = 0; i < my_items; ++i) {
-        const int item = (int)blockIdx.x + i * (int)gridDim.x;
-        const int b = item / g.Hk, hk = item % g.Hk;
-
-        // ---- steps 1-4 for the item's channels (runs under the tile loads) ----
-        const int nch = 2 * DK + g.f * g.dv;
-        for (int ch = tid; ch < nch; ch += kThreads) {
-            int c;
-            if (ch < DK) c = hk * DK + ch;
-            else if (ch < 2 * DK) c = g.Hk * DK + hk * DK + (ch - DK);
-            else c = 2 * g.Hk * DK + hk * g.f * g.dv + (ch - 2 * DK);
-            ConvWindow<T> win;
-            win.load(cin + ((size_t)b * g.D + c) * (g.K - 1), w + (size_t)c * g.K, g.K);
-            const T* x = qkv + ((size_t)b * g.D + c) * L;
-            for (int t = 0; t < L; ++t) {
-                const float y = win.push(x[t]);
-                if (ch < 2 * DK) sm.qk[t * 2 * DK + ch] = y;
-                else sm.v[t * g.f * g.dv + (ch - 2 * DK)] = y;
-                if (!IN_PLACE) {
-                    T* snap = cout + (((size_t)b * L + t) * g.D + c) * (g.K - 1);
-                    for (int e = 0; e < g.K - 1; ++e) snap[e] = win.state(e, g.K);
-                }
-            }
-            if (IN_PLACE) {
-                T* st = cout + ((size_t)b * g.D + c) * (g.K - 1);
-                for (int e = 0; e < g.K - 1; ++e) st[e] = win.state(e, g.K);
-            }
-        }
-        __syncthreads();
-        for (int t = 0; t < L; ++t) {
-            float sq = 0.f, sk = 0.f, skq = 0.f;
-            for (int e = tid; e < DK; e += kThreads) {
-                const float qv = sm.qk[t * 2 * DK + e], kv = sm.qk[t * 2 * DK + DK + e];
-                sq = fmaf(qv, qv, sq);
-                sk = fmaf(kv, kv, sk);
-                skq = fmaf(kv, qv, skq);
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                sk += __shfl_xor_sync(0xffffffffu, sk, off);
-                skq += __shfl_xor_sync(0xffffffffu, skq, off);
-            }
-            if (lane == 0) {
-                sm.nred[warp * 3 * kMaxVerify + 3 * t + 0] = sq;
-                sm.nred[warp * 3 * kMaxVerify + 3 * t + 1] = sk;
-                sm.nred[warp * 3 * kMaxVerify + 3 * t + 2] = skq;
-            }
-        }
-        __syncthreads();
-        if (tid < L) {
-            float sq = 0.f, sk = 0.f, skq = 0.f;
-#pragma unroll
-            for (int wi = 0; wi < kWarps; ++wi) {
-                sq += sm.nred[wi * 3 * kMaxVerify + 3 * tid + 0];
-                sk += sm.nred[wi * 3 * kMaxVerify + 3 * tid + 1];
-                skq += sm.nred[wi * 3 * kMaxVerify + 3 * tid + 2];
-            }
-            const float rq = g.use_l2 ? rsqrtf(sq + g.eps) : 1.f;
-            const float rk = g.use_l2 ? rsqrtf(sk + g.eps) : 1.f;
-            const float fq = __fmul_rn(g.q_scale, rq);
-            sm.coef[3 * tid + 0] = fq;
-            sm.coef[3 * tid + 1] = rk;
-            sm.coef[3 * tid + 2] = __fmul_rn(__fmul_rn(skq, fq), rk);
-        }
-        __syncthreads();
-        for (int idx = tid; idx < L * 2 * DK; idx += kThreads) {
-            const int t = idx / (2 * DK), e = idx - t * 2 * DK;
-            sm.qk[idx] = __fmul_rn(sm.qk[idx], sm.coef[3 * t + (e < DK ? 0 : 1)]);
-        }
-        __syncthreads();
-
-        // ---- step 5 over the item's tiles ----
-        for (int r = 0; r < tpi; ++r) {
-            const int j = i * tpi + r;
-            const int hl = r / nsl, col0 = (r % nsl) * kTileCols;
-            const int h = hk * g.f + hl;
-            Tile<DK> S;
-            const bool ok = mbar_wait_bounded(sm.full + (j % nstage), (uint32_t)((j / nstage) & 1));
-            if (!ok) s_abort = 1;
-            S.load_smem(sm.stage + (size_t)(j % nstage) * TILE);
-            __syncthreads();  // the stage is free again; s_abort is visible
-            if (s_abort) {
-                if (tid == 0) {
+    if (warp == kProducerWarp) {
+        // ---- producer: keep the ring nstage tiles ahead ----
+        int issued = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j % nstage;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_or_abort(empty + s, (uint32_t)(((j / nstage) & 1) ^ 1), &s_abort);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    s_abort = 1;
                     flag_device_error(&g_stream_error, 7);
-                    // let the copies still in flight land before the CTA exits
-                    for (int jj = j + 1; jj < min(ntiles, j + nstage); ++jj)
-                        mbar_wait_bounded(sm.full + (jj % nstage), (uint32_t)((jj / nstage) & 1));
                 }
+                break;
+            }
+            const TileRef tr = tile_ref(g, (int)blockIdx.x + (j / tpi) * (int)gridDim.x, j % tpi);
+            const float* src = a.S_in + ((size_t)(tr.b * g.Hv + tr.h) * DK) * g.dv + tr.col0;
+            float* dst = stage + (size_t)s * TILE;
+            if (lane == 0) {
+                fence_proxy_async_smem();  // the compute warps' reads of this stage come first
+                mbar_arrive_expect_tx(full + s, TILE * 4);
+                if (g.dv == kTileCols) bulk_g2s(dst, src, TILE * 4, full + s);
+            }
+            if (g.dv != kTileCols) {
+                __syncwarp();
+                for (int row = lane; row < DK; row += 32)
+                    bulk_g2s(dst + row * kTileCols, src + (size_t)row * g.dv, kTileCols * 4, full + s);
+            }
+            issued = j + 1;
+        }
+        // let every copy this CTA issued land before the CTA can exit
+        if (lane == 0)
+            for (int jj = max(0, issued - nstage); jj < issued; ++jj)
+                mbar_wait_bounded(full + (jj % nstage), (uint32_t)((jj / nstage) & 1));
+        return;
+    }
+
+    if (warp >= kComputeWarps) {
+        // ---- prologue: steps 1-4 for item i into buffer i % 2 ----
+        const int pt = tid - kCompute, pw = pt >> 5;
+        const T* qkv = static_cast<const T*>(a.qkv);
+        const T* w = static_cast<const T*>(a.w);
+        const T* cin = static_cast<const T*>(a.conv_in);
+        T* cout = static_cast<T*>(a.conv_out);
+        const int nch = 2 * DK + g.f * g.dv;
+        for (int i = 0; i < my_items; ++i) {
+            const int buf = i & 1;
+            if (!mbar_wait_or_abort(qempty + buf, (uint32_t)(((i >> 1) & 1) ^ 1), &s_abort)) s_pabort = 1;
+            named_sync(kBarProlog, kProlog);
+            if (s_pabort) {
+                s_abort = 1;
+                if (pt == 0) flag_device_error(&g_stream_error, 7);
                 return;
             }
-            if (warp == 0 && j + nstage < ntiles) {
-                fence_proxy_async_smem();
-                issue(j + nstage);
+            const int item = (int)blockIdx.x + i * (int)gridDim.x;
+            const int b = item / g.Hk, hk = item % g.Hk;
+            float* qk = qk_buf + (size_t)buf * L * 2 * DK;
+            float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
+            float* coef = coef_buf + buf * 3 * kMaxVerify;
+            for (int ch = pt; ch < nch; ch += kProlog) {
+                int c;
+                if (ch < DK) c = hk * DK + ch;
+                else if (ch < 2 * DK) c = g.Hk * DK + hk * DK + (ch - DK);
+                else c = 2 * g.Hk * DK + hk * g.f * g.dv + (ch - 2 * DK);
+                ConvWindow<T> win;
+                win.load(cin + ((size_t)b * g.D + c) * (g.K - 1), w + (size_t)c * g.K, g.K);
+                const T* x = qkv + ((size_t)b * g.D + c) * L;
+                for (int t = 0; t < L; ++t) {
+                    const float y = win.push(x[t]);
+                    if (ch < 2 * DK) qk[t * 2 * DK + ch] = y;
+                    else vv[t * g.f * g.dv + (ch - 2 * DK)] = y;
+                    if (!IN_PLACE) win.store_state(cout + (((size_t)b * L + t) * g.D + c) * (g.K - 1), g.K);
+                }
+                if (IN_PLACE) win.store_state(cout + ((size_t)b * g.D + c) * (g.K - 1), g.K);
             }
+            named_sync(kBarProlog, kProlog);
             for (int t = 0; t < L; ++t) {
-                const size_t gi = ((size_t)b * L + t) * g.Hv + h;
+                float sq = 0.f, sk = 0.f, skq = 0.f;
+                for (int e = pt; e < DK; e += kProlog) {
+                    const float qv = qk[t * 2 * DK + e], kv = qk[t * 2 * DK + DK + e];
+                    sq = fmaf(qv, qv, sq);
+                    sk = fmaf(kv, kv, sk);
+                    skq = fmaf(kv, qv, skq);
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                    skq += __shfl_xor_sync(0xffffffffu, skq, off);
+                }
+                if (lane == 0) {
+                    nred[pw * 3 * kMaxVerify + 3 * t + 0] = sq;
+                    nred[pw * 3 * kMaxVerify + 3 * t + 1] = sk;
+                    nred[pw * 3 * kMaxVerify + 3 * t + 2] = skq;
+                }
+            }
+            named_sync(kBarProlog, kProlog);
+            if (pt < L) {
+                float sq = 0.f, sk = 0.f, skq = 0.f;
+#pragma unroll
+                for (int wi = 0; wi < kPrologWarps; ++wi) {
+                    sq += nred[wi * 3 * kMaxVerify + 3 * pt + 0];
+                    sk += nred[wi * 3 * kMaxVerify + 3 * pt + 1];
+                    skq += nred[wi * 3 * kMaxVerify + 3 * pt + 2];
+                }
+                const float rq = g.use_l2 ? rsqrtf(sq + g.eps) : 1.f;
+                const float rk = g.use_l2 ? rsqrtf(sk + g.eps) : 1.f;
+                const float fq = __fmul_rn(g.q_scale, rq);
+                coef[3 * pt + 0] = fq;
+                coef[3 * pt + 1] = rk;
+                coef[3 * pt + 2] = __fmul_rn(__fmul_rn(skq, fq), rk);
+            }
+            named_sync(kBarProlog, kProlog);
+            for (int idx = pt; idx < L * 2 * DK; idx += kProlog) {
+                const int t = idx / (2 * DK), e = idx - t * 2 * DK;
+                qk[idx] = __fmul_rn(qk[idx], coef[3 * t + (e < DK ? 0 : 1)]);
+            }
+            named_sync(kBarProlog, kProlog);
+            if (pt == 0) mbar_arrive(qfull + buf);
+        }
+        return;
+    }
+
+    // ---- compute: step 5 on every tile of every item ----
+    int ustep = 0;  // running token-step counter: alternates the reduction buffers
+    for (int i = 0; i < my_items; ++i) {
+        const int buf = i & 1;
+        if (!mbar_wait_or_abort(qfull + buf, (uint32_t)((i >> 1) & 1), &s_abort)) s_cabort = 1;
+        const float* qk = qk_buf + (size_t)buf * L * 2 * DK;
+        const float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
+        const float* coef = coef_buf + buf * 3 * kMaxVerify;
+        for (int r = 0; r < tpi; ++r) {
+            const int j = i * tpi + r, s = j % nstage;
+            if (!mbar_wait_or_abort(full + s, (uint32_t)((j / nstage) & 1), &s_abort)) s_cabort = 1;
+            named_sync(kBarCompute, kCompute);
+            if (s_cabort) {
+                s_abort = 1;
+                if (tid == 0) flag_device_error(&g_stream_error, 7);
+                return;
+            }
+            const TileRef tr = tile_ref(g, (int)blockIdx.x + i * (int)gridDim.x, r);
+            Tile<DK> S;
+            S.load_smem(stage + (size_t)s * TILE);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);
+            for (int t = 0; t < L; ++t) {
+                const size_t gi = ((size_t)tr.b * L + t) * g.Hv + tr.h;
                 const float alpha = expf(a.gate[gi]);
                 const float bt = a.beta[gi];
                 const float4 v4 =
-                    *reinterpret_cast<const float4*>(sm.v + t * g.f * g.dv + hl * g.dv + col0 + Tile<DK>::col4());
-                const float4 o = S.step(sm.qk + t * 2 * DK + DK, sm.qk + t * 2 * DK, v4, alpha, bt,
-                                        sm.coef[3 * t + 2], sm.red + (t & 1) * kWarps * 256);
-                if (warp == 0) st_stream(a.out + gi * g.dv + col0 + Tile<DK>::col4(), o);
-                if (!IN_PLACE) S.store_global(a.S_out + (gi * DK) * g.dv + col0, g.dv);
+                    *reinterpret_cast<const float4*>(vv + t * g.f * g.dv + tr.hl * g.dv + tr.col0 + Tile<DK>::col4());
+                const float4 o = S.step(qk + t * 2 * DK + DK, qk + t * 2 * DK, v4, alpha, bt, coef[3 * t + 2],
+                                        red + (ustep & 1) * kComputeWarps * 256);
+                ++ustep;
+                if (warp == 0) st_stream(a.out + gi * g.dv + tr.col0 + Tile<DK>::col4(), o);
+                if (!IN_PLACE) S.store_global(a.S_out + (gi * DK) * g.dv + tr.col0, g.dv);
             }
-            if (IN_PLACE) S.store_global(a.S_out + ((size_t)(b * g.Hv + h) * DK) * g.dv + col0, g.dv);
+            if (IN_PLACE) S.store_global(a.S_out + ((size_t)(tr.b * g.Hv + tr.h) * DK) * g.dv + tr.col0, g.dv);
         }
-        __syncthreads();  // q/k/v buffers are rewritten by the next item
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty + buf);  // this warp is done with the item's q/k/v
     }
 }
 
@@ -310,8 +372,8 @@ bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out)
     if (g.dv % kTileCols != 0 || (g.dk != 64 && g.dk != 128)) return false;
     const int max_stage = g.dk == 64 ? 4 : 3;
     for (int ns = max_stage; ns >= 2; --ns) {
-        const size_t bytes = smem_floats(g.dk, ns, a.L, g.f, g.dv) * 4 + (size_t)ns * 8;
-        if (bytes <= 227 * 1024) {
+        const size_t bytes = Layout(g.dk, ns, a.L, g.f, g.dv).total;
+        if (bytes <= 227 * 1024 - 256) {
             *nstage_out = ns;
             *smem_out = bytes;
             return true;
