@@ -106,13 +106,14 @@ struct Tile {
 
 // Shared-memory carve-up (dynamic part).
 struct Layout {
-    size_t stage, qk, v, coef, nred, red, bars, total;
+    size_t stage, qk, v, coef, ab, nred, red, bars, total;
     __host__ __device__ Layout(int DK, int nstage, int L, int f, int dv) {
         size_t o = 0;
         stage = o; o += (size_t)nstage * DK * kTileCols * 4;
         qk = o;    o += (size_t)2 * L * 2 * DK * 4;          // double-buffered by item
         v = o;     o += (size_t)2 * L * f * dv * 4;
         coef = o;  o += (size_t)2 * 3 * kMaxVerify * 4;
+        ab = o;    o += (size_t)2 * L * f * 2 * 4;            // exp(gate), beta per token and value head
         nred = o;  o += (size_t)kPrologWarps * 3 * kMaxVerify * 4;
         red = o;   o += (size_t)2 * kComputeWarps * 256 * 4;
         bars = o;  o += (size_t)(2 * nstage + 4) * 8;         // full[ns], empty[ns], qfull[2], qempty[2]
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
     float* qk_buf = reinterpret_cast<float*>(smem_raw + lay.qk);
     float* v_buf = reinterpret_cast<float*>(smem_raw + lay.v);
     float* coef_buf = reinterpret_cast<float*>(smem_raw + lay.coef);
+    float* ab_buf = reinterpret_cast<float*>(smem_raw + lay.ab);
     float* nred = reinterpret_cast<float*>(smem_raw + lay.nred);
     float* red = reinterpret_cast<float*>(smem_raw + lay.red);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + lay.bars);
@@ -237,6 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             float* qk = qk_buf + (size_t)buf * L * 2 * DK;
             float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
             float* coef = coef_buf + buf * 3 * kMaxVerify;
+            float* ab = ab_buf + (size_t)buf * L * g.f * 2;
+            for (int idx = pt; idx < L * g.f; idx += kProlog) {
+                const int t = idx / g.f, hl = idx - t * g.f;
+                const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
+                ab[2 * idx + 0] = expf(a.gate[gi]);
+                ab[2 * idx + 1] = a.beta[gi];
+            }
             for (int ch = pt; ch < nch; ch += kProlog) {
                 int c;
                 if (ch < DK) c = hk * DK + ch;
@@ -309,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
         const float* qk = qk_buf + (size_t)buf * L * 2 * DK;
         const float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
         const float* coef = coef_buf + buf * 3 * kMaxVerify;
+        const float* ab = ab_buf + (size_t)buf * L * g.f * 2;
         for (int r = 0; r < tpi; ++r) {
             const int j = i * tpi + r, s = j % nstage;
             if (!mbar_wait_or_abort(full + s, (uint32_t)((j / nstage) & 1), &s_abort)) s_cabort = 1;
@@ -325,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             if (lane == 0) mbar_arrive(empty + s);
             for (int t = 0; t < L; ++t) {
                 const size_t gi = ((size_t)tr.b * L + t) * g.Hv + tr.h;
-                const float alpha = expf(a.gate[gi]);
-                const float bt = a.beta[gi];
+                const float alpha = ab[2 * (t * g.f + tr.hl) + 0];
+                const float bt = ab[2 * (t * g.f + tr.hl) + 1];
                 const float4 v4 =
                     *reinterpret_cast<const float4*>(vv + t * g.f * g.dv + tr.hl * g.dv + tr.col0 + Tile<DK>::col4());
                 const float4 o = S.step(qk + t * 2 * DK + DK, qk + t * 2 * DK, v4, alpha, bt, coef[3 * t + 2],
