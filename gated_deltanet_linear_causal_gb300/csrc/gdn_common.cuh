@@ -53,22 +53,22 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 }
 
 // ---- causal conv window ------------------------------------------------------
-// The last kMaxConv raw samples of one channel, newest in w[kMaxConv-1].  The
-// weights are right-aligned the same way with zeros in front, so the K-tap
-// cross-correlation (tap K-1 on the newest sample) is an 8-term FMA chain whose
-// leading terms are exact zeros.
-template <typename T>
+// The last KMAX raw samples of one channel, newest in raw[KMAX-1], for a conv
+// width K <= KMAX.  The weights are right-aligned the same way with zeros in
+// front, so the K-tap cross-correlation (tap K-1 on the newest sample) is a
+// KMAX-term FMA chain whose leading terms are exact zeros: every KMAX gives the
+// same bits for finite inputs.
+template <typename T, int KMAX = kMaxConv>
 struct ConvWindow {
-    float x[kMaxConv];
-    float w[kMaxConv];
-    T raw[kMaxConv];  // the same samples in storage type, for state write-back
+    static constexpr int kMaxConv = KMAX;
+    T raw[KMAX];    // samples in storage type (also the state written back)
+    float w[KMAX];
 
     __device__ __forceinline__ void load(const T* state, const T* weight, int K) {
 #pragma unroll
         for (int j = 0; j < kMaxConv; ++j) {
             const int s = j - (kMaxConv + 1 - K);  // index into state [K-1]
             raw[j] = (s >= 0) ? state[s] : zero_elem<T>();
-            x[j] = to_f32(raw[j]);
             const int wi = j - (kMaxConv - K);     // index into weight [K]
             w[j] = (wi >= 0) ? to_f32(weight[wi]) : 0.f;
         }
@@ -76,15 +76,11 @@ struct ConvWindow {
     // Push the next sample; return silu(conv) for the token it completes.
     __device__ __forceinline__ float push(T v) {
 #pragma unroll
-        for (int j = 0; j < kMaxConv - 1; ++j) {
-            x[j] = x[j + 1];
-            raw[j] = raw[j + 1];
-        }
+        for (int j = 0; j < kMaxConv - 1; ++j) raw[j] = raw[j + 1];
         raw[kMaxConv - 1] = v;
-        x[kMaxConv - 1] = to_f32(v);
         float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < kMaxConv; ++j) acc = fmaf(w[j], x[j], acc);
+        for (int j = 0; j < kMaxConv; ++j) acc = fmaf(w[j], to_f32(raw[j]), acc);
         return silu(acc);
     }
     // Write the K-1 sample conv state after the last push (oldest first) to dst.

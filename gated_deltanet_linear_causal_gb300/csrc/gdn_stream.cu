@@ -43,6 +43,7 @@ constexpr int kProlog = kPrologWarps * 32;
 constexpr int kThreads = (kComputeWarps + kPrologWarps + 1) * 32;
 constexpr int kBarCompute = 1, kBarProlog = 2;                  // named barrier ids
 constexpr int kTileCols = 128;
+constexpr int kStreamConv = 4;  // conv widths K <= 4 (the layer's K = 4) take this kernel
 
 template <int DK>
 struct Tile {
@@ -246,21 +247,37 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 ab[2 * idx + 0] = expf(a.gate[gi]);
                 ab[2 * idx + 1] = a.beta[gi];
             }
-            for (int ch = pt; ch < nch; ch += kProlog) {
-                int c;
-                if (ch < DK) c = hk * DK + ch;
-                else if (ch < 2 * DK) c = g.Hk * DK + hk * DK + (ch - DK);
-                else c = 2 * g.Hk * DK + hk * g.f * g.dv + (ch - 2 * DK);
-                ConvWindow<T> win;
-                win.load(cin + ((size_t)b * g.D + c) * (g.K - 1), w + (size_t)c * g.K, g.K);
-                const T* x = qkv + ((size_t)b * g.D + c) * L;
-                for (int t = 0; t < L; ++t) {
-                    const float y = win.push(x[t]);
-                    if (ch < 2 * DK) qk[t * 2 * DK + ch] = y;
-                    else vv[t * g.f * g.dv + (ch - 2 * DK)] = y;
-                    if (!IN_PLACE) win.store_state(cout + (((size_t)b * L + t) * g.D + c) * (g.K - 1), g.K);
+            // Groups of CG consecutive channels per thread, all loads of a group issued
+            // before any is used.  The Q, K and V ranges are multiples of CG long.
+            constexpr int CG = 4;
+            for (int ch0 = pt * CG; ch0 < nch; ch0 += kProlog * CG) {
+                ConvWindow<T, kStreamConv> win[CG];
+                int cc[CG];
+#pragma unroll
+                for (int u = 0; u < CG; ++u) {
+                    const int ch = ch0 + u;
+                    cc[u] = ch < DK ? hk * DK + ch
+                          : ch < 2 * DK ? g.Hk * DK + hk * DK + (ch - DK)
+                                        : 2 * g.Hk * DK + hk * g.f * g.dv + (ch - 2 * DK);
+                    win[u].load(cin + ((size_t)b * g.D + cc[u]) * (g.K - 1), w + (size_t)cc[u] * g.K, g.K);
                 }
-                if (IN_PLACE) win.store_state(cout + ((size_t)b * g.D + c) * (g.K - 1), g.K);
+                for (int t = 0; t < L; ++t) {
+                    T xt[CG];
+#pragma unroll
+                    for (int u = 0; u < CG; ++u) xt[u] = qkv[((size_t)b * g.D + cc[u]) * L + t];
+#pragma unroll
+                    for (int u = 0; u < CG; ++u) {
+                        const int ch = ch0 + u;
+                        const float y = win[u].push(xt[u]);
+                        if (ch < 2 * DK) qk[t * 2 * DK + ch] = y;
+                        else vv[t * g.f * g.dv + (ch - 2 * DK)] = y;
+                        if (!IN_PLACE) win[u].store_state(cout + (((size_t)b * L + t) * g.D + cc[u]) * (g.K - 1), g.K);
+                    }
+                }
+                if (IN_PLACE) {
+#pragma unroll
+                    for (int u = 0; u < CG; ++u) win[u].store_state(cout + ((size_t)b * g.D + cc[u]) * (g.K - 1), g.K);
+                }
             }
             named_sync(kBarProlog, kProlog);
             for (int t = 0; t < L; ++t) {
@@ -379,7 +396,7 @@ cudaError_t launch_t(const StepArgs& a, int nstage, size_t smem, cudaStream_t st
 
 bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out) {
     const Geom& g = a.g;
-    if (g.dv % kTileCols != 0 || (g.dk != 64 && g.dk != 128)) return false;
+    if (g.dv % kTileCols != 0 || (g.dk != 64 && g.dk != 128) || g.K > kStreamConv) return false;
     const int max_stage = g.dk == 64 ? 4 : 3;
     for (int ns = max_stage; ns >= 2; --ns) {
         const size_t bytes = Layout(g.dk, ns, a.L, g.f, g.dv).total;

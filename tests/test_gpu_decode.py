@@ -56,6 +56,11 @@ def test_decode_conv_widths(K):
     _run_decode_steps(synth.Shape(2, 4, 32, 32, K), "f32", batch=2, steps=K + 2, seed=40 + K, conv_kernel=K)
 
 
+@pytest.mark.parametrize("K", [1, 3])
+def test_decode_conv_widths_bulk_copy_kernel(K):
+    _run_decode_steps(synth.Shape(2, 4, 128, 128, K), "bf16", batch=3, steps=K + 2, seed=50 + K, conv_kernel=K)
+
+
 def test_decode_without_l2norm():
     _run_decode_steps(synth.Shape(2, 4, 64, 32, 4), "f32", batch=2, steps=3, seed=77, use_l2=False)
 
