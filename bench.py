@@ -55,7 +55,7 @@ def _source_sha(names):
 def _traffic(kernel_key, sources):
     """Per-launch DRAM bytes from the committed ncu summary, or None if the kernel's
     sources changed since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "stream_kernel_decode_b64.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel_key)
