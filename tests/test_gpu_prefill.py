@@ -78,14 +78,16 @@ def test_prefill_head_shapes(dk, dv, hk, hv, K):
     assert np.array_equal(f64(d["conv"]), c_r)
 
 
-def test_prefill_split_bitwise_equals_whole():
-    """Two calls with carried conv and SSM states give the bits of one call."""
+@pytest.mark.parametrize("cut", [40, 37])
+def test_prefill_split_equals_whole(cut):
+    """Two calls with carried conv and SSM states equal one call.  The kernel works in
+    blocks of 8 tokens from each call's start, so a cut on a block boundary (40)
+    reproduces the bits of one call and any other cut (37) agrees to rounding."""
     dev = device()
     shape = synth.Shape(2, 4, 64, 64, 4)
     cfg, _ = configs(shape, "bf16")
     x = synth.varlen_prefill(seed=55, shape=shape, lengths=[90])
     whole = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
-    cut = 37
     a = dict(x, cu_seqlens=np.array([0, cut], np.int32), qkv=np.ascontiguousarray(x["qkv"][:, :cut]),
              gate=x["gate"][:cut], beta=x["beta"][:cut])
     da = _prefill_dev(cfg, a, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
@@ -96,9 +98,13 @@ def test_prefill_split_bitwise_equals_whole():
              ssm_state=da["S"].cpu().numpy())
     db = _prefill_dev(cfg, b, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
     torch.cuda.synchronize()
-    assert np.array_equal(bits(torch.cat([da["out"], db["out"]])), bits(whole["out"]))
-    assert np.array_equal(bits(db["S"]), bits(whole["S"]))
+    out = torch.cat([da["out"], db["out"]])
     assert np.array_equal(bits(db["conv"]), bits(whole["conv"]))
+    if cut % 8 == 0:
+        assert np.array_equal(bits(out), bits(whole["out"]))
+        assert np.array_equal(bits(db["S"]), bits(whole["S"]))
+    else:
+        assert_parity(f64(out), f64(whole["out"]), f64(db["S"]), f64(whole["S"]), what="split vs whole")
 
 
 def _oracle_heads(ocfg, x, n, heads):
