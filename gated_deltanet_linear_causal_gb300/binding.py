@@ -228,7 +228,8 @@ def gdn_forward_prefill_noalloc(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv,
                                 ssm_state, out, stream=None):
     """Resident prefill with the library's fixed workspace (no allocation by anyone):
     for callers that cannot call cudaMalloc.  Same arguments as gdn_forward_prefill
-    minus variant and workspace; T * D * 4 must fit GDN_NOALLOC_SCRATCH_BYTES."""
+    minus variant and workspace; its T * (4 * D + 64 * Hk)-byte workspace must fit
+    GDN_NOALLOC_SCRATCH_BYTES."""
     lib = load()
     if not hasattr(lib, "_noalloc_typed"):
         vp = ctypes.c_void_p

@@ -108,44 +108,104 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrefillArgs a,
     }
 }
 
-// Block-sequential form of the gated delta rule (section 1.2, Step 5) for one
-// (sequence, value head, 16-column slice).  For a block of kBM tokens starting
-// from state S0, with G_t the running sum of the block's log-decays and
-// gamma_t = exp(G_t), unrolling Step 5 gives, per value column j:
+// ---- lagged Gram entries -------------------------------------------------------
+// For every packed token t and key head: gram[t][hk][d] = q_t . k_{t-d}
+// (d = 0..7) and gram[t][hk][8+d] = k_t . k_{t-d} (d = 1..7), from the
+// normalised rows prep_kernel wrote; entries reaching before the start of t's
+// sequence are 0.  The block kernel combines them with the decays of each
+// value head sharing the key head.
+constexpr int kBM = 8;          // tokens per block of the block-sequential kernel
+constexpr int kGramTok = 32;    // tokens per gram CTA
+
+template <int DK>
+__global__ void __launch_bounds__(256) gram_kernel(const PrefillArgs a, const float* __restrict__ y,
+                                                   float* __restrict__ gram) {
+    constexpr int KR = DK + 4;  // padded row
+    extern __shared__ float4 smem_f4[];
+    float* sk = reinterpret_cast<float*>(smem_f4);          // [kGramTok + kBM - 1][KR]  k rows
+    float* sq = sk + (kGramTok + kBM - 1) * KR;             // [kGramTok][KR]           q rows
+    __shared__ int s_start[kGramTok];
+    const Geom& g = a.g;
+    const int t0 = blockIdx.x * kGramTok, hk = blockIdx.y, tid = threadIdx.x;
+    if (tid < kGramTok && t0 + tid < a.T) s_start[tid] = a.cu[seq_of(a.cu, a.N, t0 + tid)];
+    for (int idx = tid; idx < (kGramTok + kBM - 1) * (DK / 4); idx += 256) {
+        const int r = idx / (DK / 4), c4 = idx - r * (DK / 4);
+        const int t = t0 - (kBM - 1) + r;
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t >= 0 && t < a.T) kv = __ldg(reinterpret_cast<const float4*>(y + (size_t)t * g.D + g.Hk * DK + hk * DK) + c4);
+        *reinterpret_cast<float4*>(sk + r * KR + 4 * c4) = kv;
+    }
+    for (int idx = tid; idx < kGramTok * (DK / 4); idx += 256) {
+        const int r = idx / (DK / 4), c4 = idx - r * (DK / 4);
+        const int t = t0 + r;
+        float4 qv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < a.T) qv = __ldg(reinterpret_cast<const float4*>(y + (size_t)t * g.D + hk * DK) + c4);
+        *reinterpret_cast<float4*>(sq + r * KR + 4 * c4) = qv;
+    }
+    __syncthreads();
+    // 32 tokens x 16 entries = 512 dots; 2 per thread
+    for (int job = tid; job < kGramTok * 16; job += 256) {
+        const int tl = job >> 4, e = job & 15;
+        const int t = t0 + tl;
+        if (t >= a.T) continue;
+        const int d = e & 7;
+        const bool kk = e >= 8;
+        const float* u = kk ? sk + (tl + kBM - 1) * KR : sq + tl * KR;
+        const float* v = sk + (tl + kBM - 1 - d) * KR;
+        float acc = 0.f;
+        if ((!kk || d > 0) && t - d >= s_start[tl]) {
+#pragma unroll 8
+            for (int i = 0; i < DK; ++i) acc = fmaf(u[(i + e) % DK], v[(i + e) % DK], acc);
+        }
+        gram[((size_t)t * g.Hk + hk) * 16 + e] = acc;
+    }
+}
+
+// ---- block-sequential gated delta rule (section 1.2, Step 5) -----------------
+// For a block of kBM tokens starting from state S0, with G_t the running sum of
+// the block's log-decays and gamma_t = exp(G_t), unrolling Step 5 gives, per
+// value column j:
 //   a_t     = gamma_t (S0^T k_t)_j + sum_{s<t} e^{G_t-G_s} (k_s.k_t) delta_s
 //   delta_t = beta_t (v_t - a_t)
 //   o_t     = gamma_t (S0^T q_t)_j + sum_{s<=t} e^{G_t-G_s} (k_s.q_t) delta_s
 //   S_end   = gamma_last S0 + sum_s e^{G_last-G_s} k_s delta_s^T.
-// So the 2*kBM dot products against S0 are independent (one reduction round
-// per block instead of per token), the kBM deltas are resolved per column with
-// the block's small decay-weighted Gram matrices, and S is rewritten once.
-constexpr int kBM = 8;    // tokens per block
-constexpr int kBC = 16;   // value columns per CTA
-constexpr int kBT = 128;  // threads per CTA
+// The 2*kBM dot products against S0 are independent, so each block needs one
+// reduction round instead of one per token.  One warp owns 4 value columns;
+// the 8 lanes of a column split its dk rows (16 consecutive rows each for
+// dk = 128) and reduce with shuffles only.
+constexpr int kBCW = 4;                 // columns per warp
+constexpr int kBW = 4;                  // warps per CTA
+constexpr int kBC = kBCW * kBW;         // columns per CTA
+constexpr int kBT = kBW * 32;
+
+template <int DK>
+struct BlockRows {
+    static constexpr int RPL = DK / 8;           // rows per lane
+    static constexpr int KR = DK + DK / RPL * 4;  // padded row: 4 floats after every RPL rows
+    __device__ __forceinline__ static int at(int row) { return row + (row / RPL) * 4; }
+};
 
 template <typename T, int DK>
-__global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const float* __restrict__ y) {
-    constexpr int RG = kBT / (kBC / 2);          // row groups: 16
-    constexpr int RPT = DK / RG;                 // rows per thread
+__global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const float* __restrict__ y,
+                                                    const float* __restrict__ gram) {
+    using R = BlockRows<DK>;
+    constexpr int RPL = R::RPL, KR = R::KR;
     constexpr int NV4 = (2 * DK + kBC) / 4;      // float4 per staged token: q, k, v slice
     constexpr int PER = (kBM * NV4 + kBT - 1) / kBT;
-    constexpr int QS = 2 * DK + 4;               // padded row of s_qk (q then k)
-    __shared__ __align__(16) float s_qk[kBM][QS];
+    __shared__ __align__(16) float s_q[kBM][KR], s_k[kBM][KR], s_kt[kBM][KR];
     __shared__ __align__(16) float s_v[kBM][kBC];
-    __shared__ __align__(16) float s_kt[kBM][DK];   // e^{G_last-G_s} k_s
+    __shared__ float s_gram[kBM][16];
     __shared__ float s_g[kBM], s_b[kBM], s_gam[kBM], s_c[kBM];
-    __shared__ float s_Gkk[kBM][kBM], s_Gkq[kBM][kBM];
-    __shared__ __align__(16) float s_red[RG][2 * kBM][kBC];
-    __shared__ float s_D[2 * kBM][kBC];
-    __shared__ float s_dl[kBM][kBC];
+    __shared__ __align__(16) float s_Gkk[kBM][kBM], s_Gkq[kBM][kBM];
     const Geom& g = a.g;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hk = h / g.f, col0 = slice * kBC;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int cp = tid & (kBC / 2 - 1), rg = tid / (kBC / 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cw = lane >> 3, rl = lane & 7;     // column in warp, row lane
+    const int col = warp * kBCW + cw;            // column in the CTA slice
     const int tb = a.cu[n], te = a.cu[n + 1];
     const int len = te - tb;
-    float* Sg = a.ssm_state + (size_t)(n * g.Hv + h) * DK * g.dv + col0;
+    float* Sg = a.ssm_state + (size_t)(n * g.Hv + h) * DK * g.dv + col0 + col;
 
     // New conv state of sequence n: channels split over the CTAs of the sequence.
     {
@@ -164,12 +224,12 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
     }
     if (len <= 0) return;
 
-    float2 S[RPT];
+    float S[RPL];
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) S[r] = *reinterpret_cast<const float2*>(Sg + (size_t)(rg + RG * r) * g.dv + 2 * cp);
+    for (int r = 0; r < RPL; ++r) S[r] = Sg[(size_t)(rl * RPL + r) * g.dv];
 
     float4 pre[PER];
-    float pg = 0.f, pb = 0.f;
+    float pg = 0.f, pb = 0.f, pgr = 0.f;
     auto fetch = [&](int t0) {
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
@@ -188,6 +248,8 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
         const bool ok = tid < kBM && t0 + tid < te;
         pg = ok ? a.gate[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
         pb = ok ? a.beta[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
+        pgr = (tid < kBM * 16 && t0 + (tid >> 4) < te) ? __ldg(gram + ((size_t)(t0 + (tid >> 4)) * g.Hk + hk) * 16 + (tid & 15))
+                                                      : 0.f;
     };
 
     fetch(tb);
@@ -199,7 +261,8 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
             const int idx = tid + j * kBT;
             if (idx < kBM * NV4) {
                 const int tl = idx / NV4, part = idx - tl * NV4;
-                if (part < DK / 2) *reinterpret_cast<float4*>(&s_qk[tl][4 * part]) = pre[j];
+                if (part < DK / 4) *reinterpret_cast<float4*>(&s_q[tl][R::at(4 * part)]) = pre[j];
+                else if (part < DK / 2) *reinterpret_cast<float4*>(&s_k[tl][R::at(4 * (part - DK / 4))]) = pre[j];
                 else *reinterpret_cast<float4*>(&s_v[tl][4 * (part - DK / 2)]) = pre[j];
             }
         }
@@ -207,12 +270,13 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
             s_g[tid] = pg;
             s_b[tid] = pb;
         }
+        if (tid < kBM * 16) s_gram[tid >> 4][tid & 15] = pgr;
         __syncthreads();
         if (t0 + kBM < te) fetch(t0 + kBM);  // next block's loads fly under this block
 
-        // ---- block coefficients ----
-        if (tid < 32) {
-            float G = lane < kBM ? s_g[lane] : 0.f;  // inclusive prefix sum over the block
+        // ---- block coefficients (warp 0) ----
+        if (warp == 0) {
+            float G = lane < kBM ? s_g[lane] : 0.f;  // inclusive prefix sum of the log-decays
 #pragma unroll
             for (int off = 1; off < kBM; off <<= 1) {
                 const float o = __shfl_up_sync(0xffffffffu, G, off);
@@ -222,110 +286,97 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
             if (lane < kBM) {
                 s_gam[lane] = expf(G);
                 s_c[lane] = expf(Glast - G);
-                s_g[lane] = G;  // now the running sum
+            }
+            // lane handles (t, s) pairs lane and lane + 32 of the 8x8 grid
+#pragma unroll
+            for (int p = lane; p < kBM * kBM; p += 32) {
+                const int t = p >> 3, s2 = p & 7;
+                const float Gt = __shfl_sync(0xffffffffu, G, t), Gs = __shfl_sync(0xffffffffu, G, s2);
+                const float dec = s2 <= t ? expf(Gt - Gs) : 0.f;
+                s_Gkq[t][s2] = s2 <= t ? __fmul_rn(dec, s_gram[t][t - s2]) : 0.f;
+                s_Gkk[t][s2] = s2 < t ? __fmul_rn(dec, s_gram[t][8 + t - s2]) : 0.f;
             }
         }
-        {   // Gram entries: 2 threads per (t, s) pair, each half of dk
-            const int pair = tid >> 1, half = tid & 1;
-            const int t = pair >> 3, s = pair & 7;  // 64 pairs; row 0..3 use kk, the dot of q is done too
-            float kk = 0.f, kq = 0.f;
-            for (int e = half * (DK / 2); e < (half + 1) * (DK / 2); ++e) {
-                const float ks = s_qk[s][DK + e];
-                kk = fmaf(ks, s_qk[t][DK + e], kk);
-                kq = fmaf(ks, s_qk[t][e], kq);
-            }
-            kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-            kq += __shfl_xor_sync(0xffffffffu, kq, 1);
-            __syncthreads();  // s_g holds the running sums
-            if (half == 0) {
-                const float dec = s <= t ? expf(s_g[t] - s_g[s]) : 0.f;
-                s_Gkk[t][s] = s < t ? __fmul_rn(dec, kk) : 0.f;
-                s_Gkq[t][s] = __fmul_rn(dec, kq);
-            }
-        }
-        for (int idx = tid; idx < kBM * DK; idx += kBT) {
-            const int s = idx / DK, e = idx - s * DK;
-            s_kt[s][e] = __fmul_rn(s_c[s], s_qk[s][DK + e]);
+        __syncthreads();
+        for (int idx = tid; idx < kBM * (DK / 4); idx += kBT) {
+            const int s2 = idx / (DK / 4), c4 = idx - s2 * (DK / 4);
+            const int at = R::at(4 * c4);
+            const float cs = s_c[s2];
+            float4 kv = *reinterpret_cast<const float4*>(&s_k[s2][at]);
+            kv.x = __fmul_rn(cs, kv.x); kv.y = __fmul_rn(cs, kv.y);
+            kv.z = __fmul_rn(cs, kv.z); kv.w = __fmul_rn(cs, kv.w);
+            *reinterpret_cast<float4*>(&s_kt[s2][at]) = kv;
         }
 
-        // ---- dot products against the block-start state ----
-        float pk[kBM][2], pq[kBM][2];
+        // ---- dot products of the block's keys and queries with S0 ----
+        float dk[kBM], dq[kBM];
 #pragma unroll
-        for (int t = 0; t < kBM; ++t) pk[t][0] = pk[t][1] = pq[t][0] = pq[t][1] = 0.f;
+        for (int t = 0; t < kBM; ++t) dk[t] = dq[t] = 0.f;
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            const int row = rg + RG * r;
+        for (int r4 = 0; r4 < RPL / 4; ++r4) {
+            const int at = R::at(rl * RPL + 4 * r4);
 #pragma unroll
             for (int t = 0; t < kBM; ++t) {
-                const float kv = s_qk[t][DK + row], qv = s_qk[t][row];
-                pk[t][0] = fmaf(S[r].x, kv, pk[t][0]); pk[t][1] = fmaf(S[r].y, kv, pk[t][1]);
-                pq[t][0] = fmaf(S[r].x, qv, pq[t][0]); pq[t][1] = fmaf(S[r].y, qv, pq[t][1]);
+                const float4 kv = *reinterpret_cast<const float4*>(&s_k[t][at]);
+                const float4 qv = *reinterpret_cast<const float4*>(&s_q[t][at]);
+                dk[t] = fmaf(S[4 * r4 + 0], kv.x, dk[t]); dk[t] = fmaf(S[4 * r4 + 1], kv.y, dk[t]);
+                dk[t] = fmaf(S[4 * r4 + 2], kv.z, dk[t]); dk[t] = fmaf(S[4 * r4 + 3], kv.w, dk[t]);
+                dq[t] = fmaf(S[4 * r4 + 0], qv.x, dq[t]); dq[t] = fmaf(S[4 * r4 + 1], qv.y, dq[t]);
+                dq[t] = fmaf(S[4 * r4 + 2], qv.z, dq[t]); dq[t] = fmaf(S[4 * r4 + 3], qv.w, dq[t]);
             }
         }
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) {
+#pragma unroll
+            for (int t = 0; t < kBM; ++t) {
+                dk[t] += __shfl_xor_sync(0xffffffffu, dk[t], off);
+                dq[t] += __shfl_xor_sync(0xffffffffu, dq[t], off);
+            }
+        }
+        __syncthreads();  // s_kt, s_Gkk, s_Gkq are ready
+
+        // ---- resolve the block's deltas and outputs for this lane's column ----
+        float dl[kBM];
+        float o_mine = 0.f;
 #pragma unroll
         for (int t = 0; t < kBM; ++t) {
-            *reinterpret_cast<float2*>(&s_red[rg][t][2 * cp]) = make_float2(pk[t][0], pk[t][1]);
-            *reinterpret_cast<float2*>(&s_red[rg][kBM + t][2 * cp]) = make_float2(pq[t][0], pq[t][1]);
+            float acc = __fmul_rn(s_gam[t], dk[t]);
+#pragma unroll
+            for (int s2 = 0; s2 < t; ++s2) acc = fmaf(s_Gkk[t][s2], dl[s2], acc);
+            dl[t] = t < cnt ? __fmul_rn(s_b[t], s_v[t][col] - acc) : 0.f;
+            float o = __fmul_rn(s_gam[t], dq[t]);
+#pragma unroll
+            for (int s2 = 0; s2 <= t; ++s2) o = fmaf(s_Gkq[t][s2], dl[s2], o);
+            if (t == rl) o_mine = o;
         }
-        __syncthreads();
-        for (int o = tid; o < 2 * kBM * kBC; o += kBT) {
-            const int vec = o / kBC, col = o - vec * kBC;
-            float sum = 0.f;
-#pragma unroll
-            for (int gq = 0; gq < RG; ++gq) sum += s_red[gq][vec][col];
-            s_D[vec][col] = sum;
-        }
-        __syncthreads();
-
-        // ---- resolve the block's deltas and outputs, one thread per column ----
-        if (tid < kBC) {
-            const int col = tid;
-            float dl[kBM];
-#pragma unroll
-            for (int t = 0; t < kBM; ++t) {
-                float acc = __fmul_rn(s_gam[t], s_D[t][col]);
-#pragma unroll
-                for (int s2 = 0; s2 < t; ++s2) acc = fmaf(s_Gkk[t][s2], dl[s2], acc);
-                dl[t] = t < cnt ? __fmul_rn(s_b[t], s_v[t][col] - acc) : 0.f;
-                float o = __fmul_rn(s_gam[t], s_D[kBM + t][col]);
-#pragma unroll
-                for (int s2 = 0; s2 <= t; ++s2) o = fmaf(s_Gkq[t][s2], dl[s2], o);
-                if (t < cnt) a.out[((size_t)(t0 + t) * g.Hv + h) * g.dv + col0 + col] = o;
-                s_dl[t][col] = dl[t];
-            }
-        }
-        __syncthreads();
+        if (rl < cnt) a.out[((size_t)(t0 + rl) * g.Hv + h) * g.dv + col0 + col] = o_mine;
 
         // ---- S <- gamma_last S + sum_s c_s k_s delta_s^T ----
         const float gl = s_gam[kBM - 1];
-        float d0[kBM], d1[kBM];
 #pragma unroll
-        for (int t = 0; t < kBM; ++t) {
-            d0[t] = s_dl[t][2 * cp];
-            d1[t] = s_dl[t][2 * cp + 1];
-        }
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            const int row = rg + RG * r;
-            float x = __fmul_rn(gl, S[r].x), z = __fmul_rn(gl, S[r].y);
+        for (int r4 = 0; r4 < RPL / 4; ++r4) {
+            const int at = R::at(rl * RPL + 4 * r4);
+            float x0 = __fmul_rn(gl, S[4 * r4 + 0]), x1 = __fmul_rn(gl, S[4 * r4 + 1]);
+            float x2 = __fmul_rn(gl, S[4 * r4 + 2]), x3 = __fmul_rn(gl, S[4 * r4 + 3]);
 #pragma unroll
             for (int t = 0; t < kBM; ++t) {
-                const float kt = s_kt[t][row];
-                x = fmaf(kt, d0[t], x);
-                z = fmaf(kt, d1[t], z);
+                const float4 kt = *reinterpret_cast<const float4*>(&s_kt[t][at]);
+                x0 = fmaf(kt.x, dl[t], x0); x1 = fmaf(kt.y, dl[t], x1);
+                x2 = fmaf(kt.z, dl[t], x2); x3 = fmaf(kt.w, dl[t], x3);
             }
-            S[r] = make_float2(x, z);
+            S[4 * r4 + 0] = x0; S[4 * r4 + 1] = x1; S[4 * r4 + 2] = x2; S[4 * r4 + 3] = x3;
         }
         __syncthreads();  // the block's shared data is consumed
     }
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) *reinterpret_cast<float2*>(Sg + (size_t)(rg + RG * r) * g.dv + 2 * cp) = S[r];
+    for (int r = 0; r < RPL; ++r) Sg[(size_t)(rl * RPL + r) * g.dv] = S[r];
 }
 
 template <typename T, int DK>
 cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
     const Geom& g = a.g;
     float* y = static_cast<float*>(a.ws);
+    float* gram = y + (size_t)a.T * g.D;
     const int ngrp = 2 * g.Hk + g.Hv * (g.dv / kSliceCols);
     const size_t prep_smem = (size_t)std::max(g.dk, kSliceCols) * (kPrepTokens + 1) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
@@ -333,14 +384,20 @@ cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
     prep_kernel<T><<<dim3((a.T + kPrepTokens - 1) / kPrepTokens, ngrp), kPrepThreads, prep_smem, stream>>>(a, y);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    block_kernel<T, DK><<<dim3(g.dv / kBC, g.Hv, a.N), kBT, 0, stream>>>(a, y);
+    const size_t gram_smem = (size_t)(2 * kGramTok + kBM - 1) * (DK + 4) * sizeof(float);
+    e = cudaFuncSetAttribute(gram_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
+    if (e != cudaSuccess) return e;
+    gram_kernel<DK><<<dim3((a.T + kGramTok - 1) / kGramTok, g.Hk), 256, gram_smem, stream>>>(a, y, gram);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    block_kernel<T, DK><<<dim3(g.dv / kBC, g.Hv, a.N), kBT, 0, stream>>>(a, y, gram);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t prefill_resident_workspace(const Geom& g, int /*N*/, long long T) {
-    return (size_t)T * g.D * sizeof(float);
+    return (size_t)T * g.D * sizeof(float) + (size_t)T * g.Hk * 16 * sizeof(float);
 }
 
 cudaError_t launch_prefill_resident(const PrefillArgs& a, cudaStream_t s) {

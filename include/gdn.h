@@ -162,9 +162,11 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t *cfg, int32_t num_seqs,
  * the library holds that memory until the process exits.  It calls no
  * allocator.  Arguments, layouts and results are those of gdn_forward_prefill.
  *
- *   - Limit: the workspace is T * D * 4 bytes (T = cu_seqlens_host[num_seqs]),
- *     so T * D * 4 <= GDN_NOALLOC_SCRATCH_BYTES (at D = 8192: T <= 512).
- *     Larger calls return GDN_ERR_WORKSPACE and launch nothing.
+ *   - Limit: the call needs gdn_prefill_workspace_size(cfg, num_seqs, T,
+ *     GDN_PREFILL_RESIDENT) = T * (4 * D + 64 * Hk) bytes (T =
+ *     cu_seqlens_host[num_seqs]) to fit GDN_NOALLOC_SCRATCH_BYTES (at D = 8192,
+ *     Hk = 16: T <= 496).  Larger calls return GDN_ERR_WORKSPACE and launch
+ *     nothing.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.  GDN_ERR_CUDA if the lookup

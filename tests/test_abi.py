@@ -101,7 +101,7 @@ def test_prefill_seqlens_and_workspace_validation(lib):
     assert call([0, 64], ws_bytes=16) == 9                     # workspace too small
     assert call([0, 64], variant=3) == 2
     need = binding.gdn_prefill_workspace_size(cfg, 1, 64)
-    assert need == 64 * cfg.D * 4
+    assert need == 64 * (cfg.D * 4 + cfg.num_k_heads * 64)
     assert binding.gdn_prefill_workspace_size(_cfg(io_dtype=9), 1, 64) == 0
 
 

@@ -31,7 +31,7 @@ def _states(x, dev):
 def test_noalloc_matches_the_allocating_prefill_on_two_calls():
     dev = device()
     cases = [(synth.Shape(2, 4, 64, 64, 4), [37, 100, 5, 0, 2]),   # ragged, empty and short sequences
-             (synth.PRODUCTION, [256, 200])]                       # 456 tokens at D = 8192 (14.9 MB)
+             (synth.PRODUCTION, [256, 200])]                       # 456 tokens at D = 8192 (15.4 MB)
     for n, (shape, lengths) in enumerate(cases):
         cfg, _ = configs(shape, "bf16")
         x = synth.varlen_prefill(seed=90 + n, shape=shape, lengths=lengths)
@@ -58,7 +58,7 @@ def test_noalloc_matches_the_allocating_prefill_on_two_calls():
 def test_noalloc_rejects_a_problem_larger_than_its_scratch():
     dev = device()
     cfg, _ = configs(synth.PRODUCTION, "bf16")
-    T = 513                                   # 513 * 8192 * 4 bytes > 16 MiB
+    T = 497                                   # 497 * (4 * 8192 + 64 * 16) bytes > 16 MiB
     cu = np.array([0, T], np.int32)
     x = torch.zeros(T * cfg.D, dtype=torch.bfloat16, device=dev)
     g = torch.zeros(T * 32, device=dev)
