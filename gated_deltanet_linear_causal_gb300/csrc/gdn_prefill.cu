@@ -65,21 +65,50 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrefillArgs a,
     const T* w = static_cast<const T*>(a.w);
     const T* cst = static_cast<const T*>(a.conv_state);
     const int K = g.K;
-    for (int idx = tid; idx < nch * kPrepTokens; idx += kPrepThreads) {
-        const int cl = idx / kPrepTokens, tl = idx - cl * kPrepTokens;
-        const int t = t0 + tl;
-        float v = 0.f;
-        if (t < a.T) {
-            const int c = cbase + cl, n = s_seq[tl], pos = s_pos[tl], st = s_start[tl];
-            float acc = 0.f;
-            for (int j = 0; j < K; ++j) {
-                const int p = pos - (K - 1) + j;  // position in the sequence
-                const T xv = p >= 0 ? qkv[(size_t)c * a.T + st + p] : cst[((size_t)n * g.D + c) * (K - 1) + (pos + j)];
-                acc = fmaf(to_f32(w[(size_t)c * K + j]), to_f32(xv), acc);
+    // One thread per (channel, group of kConvRun consecutive tokens): when the group
+    // lies inside one sequence past its first K-1 tokens, the K-1+kConvRun window
+    // samples and the K weights are loaded once for the whole group.
+    constexpr int kConvRun = 8;
+    for (int idx = tid; idx < nch * (kPrepTokens / kConvRun); idx += kPrepThreads) {
+        const int cl = idx / (kPrepTokens / kConvRun), tg = idx - cl * (kPrepTokens / kConvRun);
+        const int c = cbase + cl, tl0 = tg * kConvRun, t = t0 + tl0;
+        float wr[kMaxConv];
+#pragma unroll
+        for (int j = 0; j < kMaxConv; ++j) wr[j] = j < K ? to_f32(w[(size_t)c * K + j]) : 0.f;
+        const int last = min(t + kConvRun, a.T) - 1;  // last token of the group in range
+        const bool fast = t < a.T && s_seq[tl0] == s_seq[last - t0] && s_pos[tl0] >= K - 1;
+        if (fast) {
+            const T* xs = qkv + (size_t)c * a.T + t - (K - 1);
+            float xw[kConvRun + kMaxConv - 1];
+#pragma unroll
+            for (int j = 0; j < kConvRun + kMaxConv - 1; ++j)
+                xw[j] = (j < kConvRun + K - 1 && t - (K - 1) + j <= last) ? to_f32(xs[j]) : 0.f;
+#pragma unroll
+            for (int r = 0; r < kConvRun; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < kMaxConv; ++j)
+                    if (j < K) acc = fmaf(wr[j], xw[r + j], acc);
+                tile[cl * (kPrepTokens + 1) + tl0 + r] = t + r <= last ? silu(acc) : 0.f;
             }
-            v = silu(acc);
+        } else {
+            for (int r = 0; r < kConvRun; ++r) {
+                const int tl = tl0 + r, tt = t + r;
+                float v = 0.f;
+                if (tt < a.T) {
+                    const int n = s_seq[tl], pos = s_pos[tl], st = s_start[tl];
+                    float acc = 0.f;
+                    for (int j = 0; j < K; ++j) {
+                        const int p = pos - (K - 1) + j;  // position in the sequence
+                        const T xv = p >= 0 ? qkv[(size_t)c * a.T + st + p]
+                                            : cst[((size_t)n * g.D + c) * (K - 1) + (pos + j)];
+                        acc = fmaf(wr[j], to_f32(xv), acc);
+                    }
+                    v = silu(acc);
+                }
+                tile[cl * (kPrepTokens + 1) + tl] = v;
+            }
         }
-        tile[cl * (kPrepTokens + 1) + tl] = v;
     }
     __syncthreads();
     if (kind < 2) {
@@ -154,8 +183,17 @@ __global__ void __launch_bounds__(256) gram_kernel(const PrefillArgs a, const fl
         const float* v = sk + (tl + kBM - 1 - d) * KR;
         float acc = 0.f;
         if ((!kk || d > 0) && t - d >= s_start[tl]) {
+            float acc2 = 0.f;
 #pragma unroll 8
-            for (int i = 0; i < DK; ++i) acc = fmaf(u[(i + e) % DK], v[(i + e) % DK], acc);
+            for (int i = 0; i < DK; i += 8) {
+                const float4 u0 = *reinterpret_cast<const float4*>(u + i), u1 = *reinterpret_cast<const float4*>(u + i + 4);
+                const float4 v0 = *reinterpret_cast<const float4*>(v + i), v1 = *reinterpret_cast<const float4*>(v + i + 4);
+                acc = fmaf(u0.x, v0.x, acc); acc2 = fmaf(u0.y, v0.y, acc2);
+                acc = fmaf(u0.z, v0.z, acc); acc2 = fmaf(u0.w, v0.w, acc2);
+                acc = fmaf(u1.x, v1.x, acc); acc2 = fmaf(u1.y, v1.y, acc2);
+                acc = fmaf(u1.z, v1.z, acc); acc2 = fmaf(u1.w, v1.w, acc2);
+            }
+            acc += acc2;
         }
         gram[((size_t)t * g.Hk + hk) * 16 + e] = acc;
     }
@@ -170,26 +208,30 @@ __global__ void __launch_bounds__(256) gram_kernel(const PrefillArgs a, const fl
 //   o_t     = gamma_t (S0^T q_t)_j + sum_{s<=t} e^{G_t-G_s} (k_s.q_t) delta_s
 //   S_end   = gamma_last S0 + sum_s e^{G_last-G_s} k_s delta_s^T.
 // The 2*kBM dot products against S0 are independent, so each block needs one
-// reduction round instead of one per token.  One warp owns 4 value columns;
-// the 8 lanes of a column split its dk rows (16 consecutive rows each for
-// dk = 128) and reduce with shuffles only.
-constexpr int kBCW = 4;                 // columns per warp
+// reduction round instead of one per token.  The lanes of a warp that share a
+// value column split its dk rows and reduce with shuffles only (BlockCfg).
 constexpr int kBW = 4;                  // warps per CTA
-constexpr int kBC = kBCW * kBW;         // columns per CTA
 constexpr int kBT = kBW * 32;
 
+// Lane layout of the block kernel: LPC lanes share one value column and split its
+// dk rows (RPL consecutive rows each); a warp owns CPW columns, a CTA BC.  Rows
+// of the shared q/k tiles are padded by 4 floats after every RPL rows so that the
+// LPC lanes' 16-byte loads of one column group hit distinct banks.
 template <int DK>
-struct BlockRows {
-    static constexpr int RPL = DK / 8;           // rows per lane
-    static constexpr int KR = DK + DK / RPL * 4;  // padded row: 4 floats after every RPL rows
+struct BlockCfg {
+    static constexpr int LPC = DK >= 64 ? 16 : 8;
+    static constexpr int CPW = 32 / LPC;
+    static constexpr int RPL = DK / LPC;
+    static constexpr int BC = CPW * kBW;
+    static constexpr int KR = DK + LPC * 4;
     __device__ __forceinline__ static int at(int row) { return row + (row / RPL) * 4; }
 };
 
 template <typename T, int DK>
 __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const float* __restrict__ y,
                                                     const float* __restrict__ gram) {
-    using R = BlockRows<DK>;
-    constexpr int RPL = R::RPL, KR = R::KR;
+    using R = BlockCfg<DK>;
+    constexpr int RPL = R::RPL, KR = R::KR, LPC = R::LPC, CPW = R::CPW, kBC = R::BC;
     constexpr int NV4 = (2 * DK + kBC) / 4;      // float4 per staged token: q, k, v slice
     constexpr int PER = (kBM * NV4 + kBT - 1) / kBT;
     __shared__ __align__(16) float s_q[kBM][KR], s_k[kBM][KR], s_kt[kBM][KR];
@@ -201,8 +243,8 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hk = h / g.f, col0 = slice * kBC;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cw = lane >> 3, rl = lane & 7;     // column in warp, row lane
-    const int col = warp * kBCW + cw;            // column in the CTA slice
+    const int cw = lane / LPC, rl = lane % LPC;  // column in warp, row lane
+    const int col = warp * CPW + cw;             // column in the CTA slice
     const int tb = a.cu[n], te = a.cu[n + 1];
     const int len = te - tb;
     float* Sg = a.ssm_state + (size_t)(n * g.Hv + h) * DK * g.dv + col0 + col;
@@ -326,7 +368,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
             }
         }
 #pragma unroll
-        for (int off = 1; off < 8; off <<= 1) {
+        for (int off = 1; off < LPC; off <<= 1) {
 #pragma unroll
             for (int t = 0; t < kBM; ++t) {
                 dk[t] += __shfl_xor_sync(0xffffffffu, dk[t], off);
@@ -390,7 +432,7 @@ cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
     gram_kernel<DK><<<dim3((a.T + kGramTok - 1) / kGramTok, g.Hk), 256, gram_smem, stream>>>(a, y, gram);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    block_kernel<T, DK><<<dim3(g.dv / kBC, g.Hv, a.N), kBT, 0, stream>>>(a, y, gram);
+    block_kernel<T, DK><<<dim3(g.dv / BlockCfg<DK>::BC, g.Hv, a.N), kBT, 0, stream>>>(a, y, gram);
     return cudaGetLastError();
 }
 
