@@ -219,7 +219,7 @@ constexpr int kBT = kBW * 32;
 // LPC lanes' 16-byte loads of one column group hit distinct banks.
 template <int DK>
 struct BlockCfg {
-    static constexpr int LPC = DK >= 64 ? 16 : 8;
+    static constexpr int LPC = 8;  // 16 doubles the warps, and with them the per-warp delta chain
     static constexpr int CPW = 32 / LPC;
     static constexpr int RPL = DK / LPC;
     static constexpr int BC = CPW * kBW;
