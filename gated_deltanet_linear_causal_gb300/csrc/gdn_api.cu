@@ -75,7 +75,12 @@ int32_t gdn_last_cuda_error(void) { return g_last_cuda_error; }
 
 gdn_status_t gdn_device_error(int32_t* value, int32_t clear) {
     if (!value) return GDN_ERR_NULL;
-    return cuda_status(gdn::stream_error_read(value, clear != 0));
+    int32_t a = 0, b = 0;
+    gdn_status_t st = cuda_status(gdn::stream_error_read(&a, clear != 0));
+    if (st != GDN_OK) return st;
+    st = cuda_status(gdn::chunk_error_read(&b, clear != 0));
+    *value = a ? a : b;
+    return st;
 }
 
 gdn_status_t gdn_conv_state_init(const gdn_config_t* cfg, int32_t batch, void* conv_state, float* ssm_state,
@@ -198,6 +203,8 @@ size_t gdn_prefill_workspace_size(const gdn_config_t* cfg, int32_t num_seqs, int
     gdn::Geom g;
     if (check_config(cfg, &g) != GDN_OK || num_seqs < 0 || total_tokens < 0) return 0;
     if (variant == GDN_PREFILL_RESIDENT) return gdn::prefill_resident_workspace(g, num_seqs, total_tokens);
+    if (variant == GDN_PREFILL_CHUNKED && gdn::prefill_chunked_supported(g))
+        return gdn::prefill_chunked_workspace_bound(g, num_seqs, total_tokens);
     return 0;
 }
 
@@ -221,7 +228,7 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, cons
     }
     const int64_t T = cu_seqlens_host[num_seqs];
     if (T == 0) return GDN_OK;
-    if (variant == GDN_PREFILL_CHUNKED) return GDN_ERR_UNSUPPORTED;
+    if (variant == GDN_PREFILL_CHUNKED && !gdn::prefill_chunked_supported(g)) return GDN_ERR_UNSUPPORTED;
     if (!qkv || !conv_weight || !gate || !beta || (!conv_state && g.K > 1) || !ssm_state || !out) return GDN_ERR_NULL;
     const size_t eb = elem_bytes(cfg);
     if (!aligned(cu_seqlens, 4) || !aligned(qkv, 16) || !aligned(ssm_state, 16) || !aligned(out, 16) ||
@@ -246,7 +253,9 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, cons
     a.out = out;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
-    return cuda_status(gdn::launch_prefill_resident(a, reinterpret_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(variant == GDN_PREFILL_CHUNKED ? gdn::launch_prefill_chunked(a, s)
+                                                      : gdn::launch_prefill_resident(a, s));
 }
 
 }  // extern "C"

@@ -75,5 +75,13 @@ struct PrefillArgs {
 };
 size_t prefill_resident_workspace(const Geom& g, int N, long long T);
 cudaError_t launch_prefill_resident(const PrefillArgs& a, cudaStream_t stream);
+// Steps 1-4 for every packed token into token-major normalised fp32 rows y [T, D].
+cudaError_t launch_prefill_prep(const PrefillArgs& a, float* y, cudaStream_t stream);
+
+// Chunked (tensor-core) prefill, gdn_chunked.cu.
+bool prefill_chunked_supported(const Geom& g);
+size_t prefill_chunked_workspace_bound(const Geom& g, int N, long long T);
+cudaError_t launch_prefill_chunked(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t chunk_error_read(int32_t* value, bool clear);
 
 }  // namespace gdn

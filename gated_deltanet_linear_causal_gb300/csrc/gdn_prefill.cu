@@ -414,17 +414,23 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
     for (int r = 0; r < RPL; ++r) Sg[(size_t)(rl * RPL + r) * g.dv] = S[r];
 }
 
-template <typename T, int DK>
-cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
+template <typename T>
+cudaError_t launch_prep_t(const PrefillArgs& a, float* y, cudaStream_t stream) {
     const Geom& g = a.g;
-    float* y = static_cast<float*>(a.ws);
-    float* gram = y + (size_t)a.T * g.D;
     const int ngrp = 2 * g.Hk + g.Hv * (g.dv / kSliceCols);
     const size_t prep_smem = (size_t)std::max(g.dk, kSliceCols) * (kPrepTokens + 1) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
     prep_kernel<T><<<dim3((a.T + kPrepTokens - 1) / kPrepTokens, ngrp), kPrepThreads, prep_smem, stream>>>(a, y);
-    e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+template <typename T, int DK>
+cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
+    const Geom& g = a.g;
+    float* y = static_cast<float*>(a.ws);
+    float* gram = y + (size_t)a.T * g.D;
+    cudaError_t e = launch_prep_t<T>(a, y, stream);
     if (e != cudaSuccess) return e;
     const size_t gram_smem = (size_t)(2 * kGramTok + kBM - 1) * (DK + 4) * sizeof(float);
     e = cudaFuncSetAttribute(gram_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
@@ -437,6 +443,10 @@ cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_prefill_prep(const PrefillArgs& a, float* y, cudaStream_t s) {
+    return a.g.io_bf16 ? launch_prep_t<__nv_bfloat16>(a, y, s) : launch_prep_t<float>(a, y, s);
+}
 
 size_t prefill_resident_workspace(const Geom& g, int /*N*/, long long T) {
     return (size_t)T * g.D * sizeof(float) + (size_t)T * g.Hk * 16 * sizeof(float);

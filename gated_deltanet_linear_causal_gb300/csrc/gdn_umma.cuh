@@ -1,0 +1,139 @@
+// gdn_umma.cuh -- 5th-generation tensor-core helpers (tcgen05, sm_100+): shared
+// memory operand layout, descriptors, MMA issue, commit and TMEM access.
+//
+// Operands live in shared memory in the canonical no-swizzle layout: 8x8 bf16
+// "core matrices" of 128 contiguous bytes (8 rows x 16 bytes).  A K-major
+// operand of R rows x Ktot columns places element (r, k) at
+//   (r/8)*(Ktot/8)*128 + (k/8)*128 + (r%8)*16 + (k%8)*2,
+// so the descriptor's leading-dimension offset (next core matrix along K) is
+// 128 bytes and its stride-dimension offset (next 8 rows) is (Ktot/8)*128.  The
+// same bytes read as an MN-major operand (rows become K, columns become M) take
+// LBO = (Ktot/8)*128 and SBO = 128.
+//
+// fp32 values enter the tensor core as bf16 hi/lo pairs (x = hi + lo + O(2^-16 x)):
+// an operand stores its hi part at columns [0, K) and its lo part at [K, 2K), and
+// a product accumulates hi*hi + hi*lo + lo*hi in fp32, which keeps about 16
+// significant bits per operand instead of bf16's 8.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_tma.cuh"
+
+namespace gdn {
+namespace umma {
+
+__device__ __forceinline__ uint32_t kmajor_offset(int r, int k, int ktot) {
+    return (uint32_t)((r >> 3) * (ktot >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// Store fp32 x at (r, k) of a split operand with K logical columns (ktot = 2K).
+__device__ __forceinline__ void store_split(unsigned char* base, int r, int k, int K, float x) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    *reinterpret_cast<__nv_bfloat16*>(base + kmajor_offset(r, k, 2 * K)) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(base + kmajor_offset(r, K + k, 2 * K)) = lo;
+}
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+// kind::f16 instruction descriptor: bf16 A and B, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// D (+)= A * B^T over K logical columns, both operands split (ktot = 2K) and K-major;
+// A has M rows, B has N rows.  Issued by one thread.
+__device__ __forceinline__ void mma_split_kk(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
+                                             int N, int K, bool accumulate) {
+    const uint32_t idesc = idesc_bf16(M, N);
+    const uint32_t sbo = (uint32_t)(2 * K / 8) * 128;
+    const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+    bool acc = accumulate;
+#pragma unroll
+    for (int pr = 0; pr < 3; ++pr) {  // (hi, hi), (hi, lo), (lo, hi)
+        const int pa = pr == 2, pb = pr == 1;
+        for (int ks = 0; ks < K / 16; ++ks) {
+            const uint32_t ka = (uint32_t)((pa * K + 16 * ks) / 8) * 128;
+            const uint32_t kb = (uint32_t)((pb * K + 16 * ks) / 8) * 128;
+            mma_bf16(d_tmem, smem_desc(sa + ka, 128, sbo), smem_desc(sb + kb, 128, sbo), idesc, acc);
+            acc = true;
+        }
+    }
+}
+
+// D (+)= A^T * B^T where A is stored K-major as [Kdim rows][M columns] split over
+// its columns (ktot_a = 2M) and read MN-major; B is K-major [N rows][2*Kdim].
+__device__ __forceinline__ void mma_split_mn(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
+                                             int N, int Kdim, bool accumulate) {
+    const uint32_t idesc = idesc_bf16(M, N, true);
+    const uint32_t a_kstep = (uint32_t)(2 * M / 8) * 128;  // next 8 rows of the stored A (= next 8 along K)
+    const uint32_t b_sbo = (uint32_t)(2 * Kdim / 8) * 128;
+    const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+    bool acc = accumulate;
+#pragma unroll
+    for (int pr = 0; pr < 3; ++pr) {
+        const int pa = pr == 2, pb = pr == 1;
+        for (int ks = 0; ks < Kdim / 16; ++ks) {
+            const uint32_t oa = (uint32_t)(2 * ks) * a_kstep + (uint32_t)(pa * M / 8) * 128;
+            const uint32_t ob = (uint32_t)((pb * Kdim + 16 * ks) / 8) * 128;
+            mma_bf16(d_tmem, smem_desc(sa + oa, a_kstep, 128), smem_desc(sb + ob, 128, b_sbo), idesc, acc);
+            acc = true;
+        }
+    }
+}
+
+__device__ __forceinline__ void commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// One warp: allocate ncols TMEM columns (power of two >= 32); the address lands in *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 32 consecutive fp32 columns of TMEM lane (warp's sub-partition base + lane id).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// TMEM address of row `row` of an accumulator at column `col`: M = 128 puts row r
+// in lane r; M = 64 puts row r in lane (r % 16) + 32 * (r / 16).
+__device__ __forceinline__ uint32_t lane_of(int row, int M) { return M == 128 ? (uint32_t)row : (uint32_t)((row & 15) + 32 * (row >> 4)); }
+
+}  // namespace umma
+}  // namespace gdn

@@ -135,7 +135,9 @@ size_t gdn_prefill_workspace_size(const gdn_config_t *cfg, int32_t num_seqs,
  *   conv_state       device [num_seqs, D, K-1] io dtype, in/out
  *   ssm_state        device [num_seqs, Hv, dk, dv] fp32, in/out
  *   out              device [T, Hv, dv] fp32
- *   variant          GDN_PREFILL_RESIDENT or GDN_PREFILL_CHUNKED
+ *   variant          GDN_PREFILL_RESIDENT (any supported shape) or
+ *                    GDN_PREFILL_CHUNKED (tensor cores; head_k_dim = 128 only,
+ *                    GDN_ERR_UNSUPPORTED otherwise)
  *   workspace        device scratch of at least gdn_prefill_workspace_size()
  *                    bytes, 16-byte aligned, not shared with a concurrent call
  * Empty sequences (cu[n] == cu[n+1]) keep their states.  T = 0 is a no-op.

@@ -127,14 +127,18 @@ def _oracle_heads(ocfg, x, n, heads):
     return res
 
 
-def test_prefill_long_production_sampled_heads():
+BOTH = [gb.GDN_PREFILL_RESIDENT, gb.GDN_PREFILL_CHUNKED]
+
+
+@pytest.mark.parametrize("variant", BOTH, ids=["resident", "chunked"])
+def test_prefill_long_production_sampled_heads(variant):
     """B=1, L=8192, H_k=16, H_v=32, d=128, slow decay: the whole layer on the GPU;
     the oracle recomputes value heads 0, 13 and 31 over the full sequence."""
     dev = device()
     shape = synth.PRODUCTION
     cfg, ocfg = configs(shape, "bf16")
     x = synth.long_prefill(seed=3)
-    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    d = _prefill_dev(cfg, x, dev, variant, "bf16")
     ref = _oracle_heads(ocfg, x, 0, [0, 13, 31])
     torch.cuda.synchronize()
     out, S = f64(d["out"]), f64(d["S"])
@@ -145,14 +149,15 @@ def test_prefill_long_production_sampled_heads():
     assert np.array_equal(f64(d["conv"])[0], tail), "conv state = last K-1 raw inputs"
 
 
-def test_prefill_varlen_production_sampled():
+@pytest.mark.parametrize("variant", BOTH, ids=["resident", "chunked"])
+def test_prefill_varlen_production_sampled(variant):
     """16 sequences with lengths U{256..2048}, random per-sequence states: the oracle
     recomputes 3 sequences x 3 value heads."""
     dev = device()
     shape = synth.PRODUCTION
     cfg, ocfg = configs(shape, "bf16")
     x = synth.varlen_prefill(seed=4)
-    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    d = _prefill_dev(cfg, x, dev, variant, "bf16")
     torch.cuda.synchronize()
     out, S = f64(d["out"]), f64(d["S"])
     cu = x["cu_seqlens"]
@@ -160,6 +165,47 @@ def test_prefill_varlen_production_sampled():
         for h, (o_r, S_r) in _oracle_heads(ocfg, x, n, [1, 16, 30]).items():
             assert_parity(out[cu[n]:cu[n + 1], h], o_r, S[n, h], S_r, what=f"seq {n} head {h}")
         assert np.array_equal(f64(d["conv"])[n], f64(x["qkv"][:, cu[n + 1] - 3:cu[n + 1]]))
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("hv,dv", [(4, 64), (2, 32), (8, 96)])
+def test_prefill_chunked_ragged(io, hv, dv):
+    """The tensor-core chunked form (d_k = 128, 64-token chunks): empty sequences,
+    sequences shorter than the conv window, chunk-aligned and ragged tails, several
+    GQA ratios, every output and state against the oracle."""
+    dev = device()
+    shape = synth.Shape(2, hv, 128, dv, 4)
+    cfg, ocfg = configs(shape, io)
+    lengths = [0, 1, 2, 3, 17, 64, 65, 130, 0, 200, 5]
+    x = synth.varlen_prefill(seed=70 + hv + dv, shape=shape, lengths=lengths)
+    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_CHUNKED, io)
+    o_r, c_r, S_r = _oracle_prefill(ocfg, x)
+    torch.cuda.synchronize()
+    assert_parity(f64(d["out"]), o_r, f64(d["S"]), S_r, what="chunked")
+    assert np.array_equal(f64(d["conv"]), c_r)
+
+
+def test_prefill_chunked_matches_resident():
+    """Both prefill forms agree to rounding on the same inputs (fast decay, random states)."""
+    dev = device()
+    shape = synth.Shape(4, 8, 128, 128, 4)
+    cfg, _ = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=81, shape=shape, lengths=[300, 1, 129])
+    r = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, "bf16")
+    c = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_CHUNKED, "bf16")
+    torch.cuda.synchronize()
+    assert_parity(f64(c["out"]), f64(r["out"]), f64(c["S"]), f64(r["S"]), what="chunked vs resident")
+    assert torch.equal(c["conv"], r["conv"])
+
+
+def test_prefill_chunked_rejects_other_head_sizes():
+    dev = device()
+    shape = synth.Shape(2, 4, 64, 64, 4)
+    cfg, _ = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=5, shape=shape, lengths=[10])
+    with pytest.raises(gb.GdnError) as e:
+        _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_CHUNKED, "bf16")
+    assert e.value.status == 8
 
 
 def test_prefill_empty_is_noop():
