@@ -398,18 +398,21 @@ def main():
     sec = {}
     if secondary and rank == 0:
         shape = synth.PRODUCTION
-        med, times = run_prefill(dev, x_long, gb.GDN_PREFILL_RESIDENT)
-        nb = prefill_bytes(shape, x_long["cu_seqlens"], False)
-        sec["prefill_L8192"] = {"variant": "resident", "tokens_per_s": round(8192 / (med / 1e3), 1),
-                                "ms": round(med, 4), "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
-        med, _ = run_prefill(dev, x_var, gb.GDN_PREFILL_RESIDENT)
-        T = int(x_var["cu_seqlens"][-1])
-        nb = prefill_bytes(shape, x_var["cu_seqlens"], True)
-        sec["prefill_varlen16"] = {"variant": "resident", "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
-                                   "ms": round(med, 4),
-                                   "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                   "algorithmic_bytes": nb, "launches": 2, "cold_l2": True}
+        for name, variant in (("chunked", gb.GDN_PREFILL_CHUNKED), ("resident", gb.GDN_PREFILL_RESIDENT)):
+            key = "" if name == "chunked" else "_resident"
+            med, times = run_prefill(dev, x_long, variant)
+            nb = prefill_bytes(shape, x_long["cu_seqlens"], False)
+            sec["prefill_L8192" + key] = {"variant": name, "tokens_per_s": round(8192 / (med / 1e3), 1),
+                                          "ms": round(med, 4),
+                                          "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                          "algorithmic_bytes": nb, "cold_l2": True}
+            med, _ = run_prefill(dev, x_var, variant)
+            T = int(x_var["cu_seqlens"][-1])
+            nb = prefill_bytes(shape, x_var["cu_seqlens"], True)
+            sec["prefill_varlen16" + key] = {"variant": name, "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
+                                             "ms": round(med, 4),
+                                             "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                             "algorithmic_bytes": nb, "cold_l2": True}
         mv, mc = run_verify(dev, x_ver)
         nb = verify_bytes(shape, 32, 4)
         sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4),
