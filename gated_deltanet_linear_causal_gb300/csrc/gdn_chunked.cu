@@ -182,30 +182,55 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
             Pb[t * (kC + 1) + s] = __fmul_rn(dec, qk[t * (kC + 1) + s]);
         }
         __syncthreads();
+        // T = (I + A)^-1, A strictly lower: blocked by 16.  Diagonal blocks by forward
+        // substitution (one thread per column of each block), then the block
+        // sub-diagonals d = 1, 2, 3: T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj.
+        constexpr int BB = 16, NB = kC / BB;
         if (tid < kC) {
-            // column u of T = (I + A)^-1 by forward substitution; columns are independent
-            const int u = tid;
-            for (int i = 0; i < kC; ++i) {
+            const int blk = tid / BB, u = tid % BB, o = blk * BB;
+            for (int i = 0; i < BB; ++i) {
                 float v = i == u ? 1.f : 0.f;
                 if (i > u) {
-                    float a0 = 0.f, a1 = 0.f;
-                    int s = u;
-                    for (; s + 1 < i; s += 2) {
-                        a0 = fmaf(Ab[i * (kC + 1) + s], Tb[s * (kC + 1) + u], a0);
-                        a1 = fmaf(Ab[i * (kC + 1) + s + 1], Tb[(s + 1) * (kC + 1) + u], a1);
-                    }
-                    if (s < i) a0 = fmaf(Ab[i * (kC + 1) + s], Tb[s * (kC + 1) + u], a0);
-                    v = -(a0 + a1);
+                    float acc = 0.f;
+                    for (int s2 = u; s2 < i; ++s2) acc = fmaf(Ab[(o + i) * (kC + 1) + o + s2], Tb[(o + s2) * (kC + 1) + o + u], acc);
+                    v = -acc;
                 }
-                Tb[i * (kC + 1) + u] = v;
+                Tb[(o + i) * (kC + 1) + o + u] = v;
             }
+            for (int i = 0; i < BB; ++i)  // zero the block row's entries right of the diagonal
+                for (int jb = blk + 1; jb < NB; ++jb) Tb[(o + i) * (kC + 1) + jb * BB + u] = 0.f;
         } else {
             for (int idx = tid - kC; idx < kC * kC; idx += kCT - kC) {
-                const int t = idx / kC, s = idx - t * kC;
-                umma::store_split(img + kTBytes, t, s, kC, Pb[t * (kC + 1) + s]);
+                const int t = idx / kC, s2 = idx - t * kC;
+                umma::store_split(img + kTBytes, t, s2, kC, Pb[t * (kC + 1) + s2]);
             }
         }
         __syncthreads();
+        // scratch [NB-1][16][16] in the T half of the image buffer, which is written last
+        float* Xb = reinterpret_cast<float*>(img);
+        for (int d = 1; d < NB; ++d) {
+            const int npair = NB - d;
+            // X_p = sum_{k=j}^{i-1} A_ik T_kj for pair p: (i, j) = (j + d, j), j = p
+            for (int idx = tid; idx < npair * BB * BB; idx += kCT) {
+                const int p = idx / (BB * BB), r = (idx / BB) % BB, cc = idx % BB;
+                const int bi = p + d, bj = p;
+                float acc = 0.f;
+                for (int kb = bj; kb < bi; ++kb)
+                    for (int m = 0; m < BB; ++m)
+                        acc = fmaf(Ab[(bi * BB + r) * (kC + 1) + kb * BB + m], Tb[(kb * BB + m) * (kC + 1) + bj * BB + cc], acc);
+                Xb[idx] = acc;
+            }
+            __syncthreads();
+            for (int idx = tid; idx < npair * BB * BB; idx += kCT) {
+                const int p = idx / (BB * BB), r = (idx / BB) % BB, cc = idx % BB;
+                const int bi = p + d, bj = p;
+                float acc = 0.f;
+                for (int m = 0; m <= r; ++m)
+                    acc = fmaf(Tb[(bi * BB + r) * (kC + 1) + bi * BB + m], Xb[p * BB * BB + m * BB + cc], acc);
+                Tb[(bi * BB + r) * (kC + 1) + bj * BB + cc] = -acc;
+            }
+            __syncthreads();
+        }
         for (int idx = tid; idx < kC * kC; idx += kCT) {
             const int t = idx / kC, s = idx - t * kC;
             umma::store_split(img, t, s, kC, Tb[t * (kC + 1) + s]);
@@ -219,6 +244,10 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
 }
 
 // ---- chain ----------------------------------------------------------------------
+// Loads run ahead of the rounds: T and P are double-buffered (chunk c+1's copy is
+// issued when chunk c starts), Q for chunk c+1 is copied as soon as round 1 of
+// chunk c has read it, K as soon as round 3 has, and the V slice and gates of
+// chunk c+1 are fetched into registers while chunk c computes.
 template <typename T>
 __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, const float* __restrict__ y,
                                                        const int32_t* __restrict__ coff,
@@ -227,15 +256,15 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* ktok = smem;                        // 32 KB  K   [64 tok][2*128]
     unsigned char* qtok = ktok + kKTokBytes;           // 32 KB  Q   [64 tok][2*128]
-    unsigned char* tpi = qtok + kKTokBytes;            // 32 KB  T, P [64][2*64]
-    unsigned char* s0t = tpi + kTPBytes;               // 16 KB  S0^T [32 cols][2*128]
+    unsigned char* tpb = qtok + kKTokBytes;            // 2 x 32 KB  T, P [64][2*64]
+    unsigned char* s0t = tpb + 2 * kTPBytes;           // 16 KB  S0^T [32 cols][2*128]
     unsigned char* rt = s0t + kNS * 2 * kDK * 2;       //  8 KB  R^T  [32][2*64]
     unsigned char* ut = rt + kNS * 2 * kC * 2;         //  8 KB  U^T
     unsigned char* cut = ut + kNS * 2 * kC * 2;        //  8 KB  (diag(c) U)^T
     float* vv = reinterpret_cast<float*>(cut + kNS * 2 * kC * 2);  // [64][32]
     __shared__ float s_g[kC], s_b[kC], s_G[kC], s_carry;
     __shared__ uint32_t s_tmem;
-    __shared__ __align__(8) uint64_t s_ld, s_mma;
+    __shared__ __align__(8) uint64_t s_k, s_q, s_tp[2], s_mma;
     __shared__ int s_abort;
     const Geom& g = a.g;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
@@ -259,6 +288,8 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             }
     }
     if (len <= 0) return;
+    const int nchunks = coff[n + 1] - coff[n];
+    const int chunk0 = coff[n];
 
     // state rows: thread i holds row i (key dim) of the 32-column slice
     float* Sg = a.ssm_state + ((size_t)(n * g.Hv + h) * kDK + tid) * g.dv + col0;
@@ -273,7 +304,10 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 
     if (warp == 0) umma::tmem_alloc(&s_tmem, 256);
     if (tid == 0) {
-        mbar_init(&s_ld, 1);
+        mbar_init(&s_k, 1);
+        mbar_init(&s_q, 1);
+        mbar_init(&s_tp[0], 1);
+        mbar_init(&s_tp[1], 1);
         mbar_init(&s_mma, 1);
         fence_mbar_init();
         s_abort = 0;
@@ -285,39 +319,66 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     const uint32_t tDk = tmem + 0, tDq = tmem + 32, tU = tmem + 64, tO = tmem + 96, tS = tmem + 128;
     const uint32_t wl = (uint32_t)(32 * warp) << 16;   // this warp's TMEM lane base
     const int trow = 16 * warp + (lane & 15);         // M = 64 accumulator row held by lanes 0-15
-    uint32_t ph_ld = 0, ph_mma = 0;
-    bool ld_pending = false, mma_pending = false;  // thread 0's view, for a clean exit on abort
 
-    const int nchunks = coff[n + 1] - coff[n];
+    // thread 0's bookkeeping of copies and MMAs in flight (for a clean exit on abort)
+    int k_iss = 0, q_iss = 0, tp_iss[2] = {0, 0}, mma_iss = 0;
+    auto load_k = [&](int c) {
+        mbar_arrive_expect_tx(&s_k, kKTokBytes);
+        bulk_g2s(ktok, kq + ((size_t)(chunk0 + c) * g.Hk + hk) * kKQBytes, kKTokBytes, &s_k);
+        ++k_iss;
+    };
+    auto load_q = [&](int c) {
+        mbar_arrive_expect_tx(&s_q, kKTokBytes);
+        bulk_g2s(qtok, kq + ((size_t)(chunk0 + c) * g.Hk + hk) * kKQBytes + kKTokBytes, kKTokBytes, &s_q);
+        ++q_iss;
+    };
+    auto load_tp = [&](int c) {
+        const int b = c & 1;
+        mbar_arrive_expect_tx(&s_tp[b], kTPBytes);
+        bulk_g2s(tpb + b * kTPBytes, tp + ((size_t)(chunk0 + c) * g.Hv + h) * kTPBytes, kTPBytes, &s_tp[b]);
+        ++tp_iss[b];
+    };
+    // V slice (16 values per thread) and gates of a chunk, into registers
+    float pv[kC * kNS / kCT], pg = 0.f, pb = 0.f;
+    auto fetch = [&](int c) {
+        const int t0 = tb + c * kC, cnt = min(kC, te - t0);
+#pragma unroll
+        for (int k = 0; k < kC * kNS / kCT; ++k) {
+            const int idx = tid + k * kCT, t = idx / kNS, j = idx - t * kNS;
+            pv[k] = t < cnt ? y[(size_t)(t0 + t) * g.D + 2 * g.Hk * kDK + h * g.dv + col0 + j] : 0.f;
+        }
+        const bool in = tid < cnt;
+        pg = tid < kC && in ? a.gate[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
+        pb = tid < kC && in ? a.beta[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        if (!mbar_wait_bounded(bar, parity)) s_abort = 1;
+    };
+
+    if (tid == 0) {
+        load_k(0);
+        load_q(0);
+        load_tp(0);
+    }
+    fetch(0);
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = tb + c * kC, cnt = min(kC, te - t0);
-        const int chunk = coff[n] + c;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&s_ld, kKQBytes + kTPBytes);
-            bulk_g2s(ktok, kq + ((size_t)chunk * g.Hk + hk) * kKQBytes, kKQBytes, &s_ld);
-            bulk_g2s(tpi, tp + ((size_t)chunk * g.Hv + h) * kTPBytes, kTPBytes, &s_ld);
-            ld_pending = true;
-        }
-        // V slice, gates and decays of the chunk
-        for (int idx = tid; idx < kC * kNS; idx += kCT) {
-            const int t = idx / kNS, j = idx - t * kNS;
-            vv[idx] = t < cnt ? y[(size_t)(t0 + t) * g.D + 2 * g.Hk * kDK + h * g.dv + col0 + j] : 0.f;
-        }
+        const unsigned char* tpi = tpb + (c & 1) * kTPBytes;
+        if (tid == 0 && c + 1 < nchunks) load_tp(c + 1);  // its buffer's last reader, chunk c-1, is done
+#pragma unroll
+        for (int k = 0; k < kC * kNS / kCT; ++k) vv[tid + k * kCT] = pv[k];
         if (tid < kC) {
-            const bool in = tid < cnt;
-            s_g[tid] = in ? a.gate[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
-            s_b[tid] = in ? a.beta[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
+            s_g[tid] = pg;
+            s_b[tid] = pb;
         }
         __syncthreads();
+        if (c + 1 < nchunks) fetch(c + 1);
         scan64(s_g, s_G, &s_carry);  // running log-decay; ends with a barrier
 
         // ---- round 1: K S0 and Q S0 ----
-        if (mbar_wait_bounded(&s_ld, ph_ld)) {
-            ph_ld ^= 1;
-            ld_pending = false;
-        } else {
-            s_abort = 1;
-        }
+        wait_all(&s_k, (uint32_t)(c & 1));
+        wait_all(&s_q, (uint32_t)(c & 1));
+        wait_all(&s_tp[c & 1], (uint32_t)((c >> 1) & 1));
         fence_proxy_async_smem();  // s0t was written by the generic proxy
         umma::fence_before_sync();
         __syncthreads();
@@ -327,15 +388,11 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             umma::mma_split_kk(tDk, ktok, s0t, kC, kNS, kDK, false);
             umma::mma_split_kk(tDq, qtok, s0t, kC, kNS, kDK, false);
             umma::commit(&s_mma);
-            mma_pending = true;
+            ++mma_iss;
         }
-        if (mbar_wait_bounded(&s_mma, ph_mma)) {
-            ph_mma ^= 1;
-            mma_pending = false;
-        } else {
-            s_abort = 1;
-        }
+        wait_all(&s_mma, (uint32_t)((3 * c) & 1));
         umma::fence_after_sync();
+        if (tid == 0 && c + 1 < nchunks) load_q(c + 1);  // round 1 was Q's last reader
         float dk[kNS], dq[kNS];
         umma::tmem_ld32(tDk + wl, dk);
         umma::tmem_ld32(tDq + wl, dq);
@@ -356,14 +413,9 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         if (tid == 0) {
             umma::mma_split_kk(tU, tpi, rt, kC, kNS, kC, false);
             umma::commit(&s_mma);
-            mma_pending = true;
+            ++mma_iss;
         }
-        if (mbar_wait_bounded(&s_mma, ph_mma)) {
-            ph_mma ^= 1;
-            mma_pending = false;
-        } else {
-            s_abort = 1;
-        }
+        wait_all(&s_mma, (uint32_t)((3 * c + 1) & 1));
         umma::fence_after_sync();
         float uu[kNS];
         umma::tmem_ld32(tU + wl, uu);
@@ -386,15 +438,11 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             umma::mma_split_kk(tO, tpi + kTBytes, ut, kC, kNS, kC, false);
             umma::mma_split_mn(tS, ktok, cut, kDK, kNS, kC, false);
             umma::commit(&s_mma);
-            mma_pending = true;
+            ++mma_iss;
         }
-        if (mbar_wait_bounded(&s_mma, ph_mma)) {
-            ph_mma ^= 1;
-            mma_pending = false;
-        } else {
-            s_abort = 1;
-        }
+        wait_all(&s_mma, (uint32_t)((3 * c + 2) & 1));
         umma::fence_after_sync();
+        if (tid == 0 && c + 1 < nchunks) load_k(c + 1);  // round 3 was K's last reader
         float oo[kNS], ss[kNS];
         umma::tmem_ld32(tO + wl, oo);
         umma::tmem_ld32(tS + wl, ss);
@@ -415,14 +463,19 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             umma::store_split(s0t, j, tid, kDK, S[j]);
         }
         umma::fence_before_sync();
-        __syncthreads();  // all operand reads of this chunk are complete before the next loads
+        __syncthreads();  // this chunk's operand reads are complete
+        if (s_abort) break;
         umma::fence_after_sync();
     }
     if (s_abort && tid == 0) {
         flag_device_error(&g_chunk_error, 7);
-        // let a bulk copy or an MMA still in flight finish before TMEM and smem are released
-        if (ld_pending) mbar_wait_bounded(&s_ld, ph_ld);
-        if (mma_pending) mbar_wait_bounded(&s_mma, ph_mma);
+        // let copies and MMAs still in flight land before TMEM and shared memory are released:
+        // wait for the last issued phase of each barrier (a completed phase returns at once)
+        if (k_iss) mbar_wait_bounded(&s_k, (uint32_t)((k_iss - 1) & 1));
+        if (q_iss) mbar_wait_bounded(&s_q, (uint32_t)((q_iss - 1) & 1));
+        for (int b = 0; b < 2; ++b)
+            if (tp_iss[b]) mbar_wait_bounded(&s_tp[b], (uint32_t)((tp_iss[b] - 1) & 1));
+        if (mma_iss) mbar_wait_bounded(&s_mma, (uint32_t)((mma_iss - 1) & 1));
     }
     umma::fence_before_sync();
     __syncthreads();
@@ -432,7 +485,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     for (int j = 0; j < kNS; j += 4) *reinterpret_cast<float4*>(Sg + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
 }
 
-constexpr size_t kChainSmem = 2 * kKTokBytes + kTPBytes + kNS * 2 * kDK * 2 + 3 * (kNS * 2 * kC * 2) + kC * kNS * 4;
+constexpr size_t kChainSmem = 2 * kKTokBytes + 2 * kTPBytes + kNS * 2 * kDK * 2 + 3 * (kNS * 2 * kC * 2) + kC * kNS * 4;
 constexpr size_t kPrepSmem = kKQBytes + 3 * kC * (kC + 1) * 4 + kTPBytes;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
