@@ -96,10 +96,11 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
     unsigned char* qtok = smem + kKTokBytes;                            // 32 KB
     float* kk = reinterpret_cast<float*>(smem);                         // [64][65], after the MMAs
     float* qk = kk + kC * (kC + 1);                                     // [64][65]
-    float* Ab = reinterpret_cast<float*>(smem + kKQBytes);              // [64][65]
-    float* Pb = Ab + kC * (kC + 1);                                     // [64][65]
-    float* Tb = Pb + kC * (kC + 1);                                     // [64][65]
-    unsigned char* img = reinterpret_cast<unsigned char*>(Tb + kC * (kC + 1));  // T and P images, 32 KB
+    // after the MMAs: kk, qk [64][65] over the images, then A and T [64][65] and the
+    // T and P operand images (32 KB)
+    float* Ab = qk + kC * (kC + 1);
+    float* Tb = Ab + kC * (kC + 1);
+    unsigned char* img = reinterpret_cast<unsigned char*>(Tb + kC * (kC + 1));
     __shared__ float s_g[kC], s_b[kC], s_G[kC], s_carry;
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_bar;
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
             const int t = idx / kC, s = idx - t * kC;
             const float dec = s <= t ? expf(s_G[t] - s_G[s]) : 0.f;
             Ab[t * (kC + 1) + s] = s < t ? __fmul_rn(__fmul_rn(s_b[t], dec), kk[t * (kC + 1) + s]) : 0.f;
-            Pb[t * (kC + 1) + s] = __fmul_rn(dec, qk[t * (kC + 1) + s]);
+            umma::store_split(img + kTBytes, t, s, kC, __fmul_rn(dec, qk[t * (kC + 1) + s]));  // P
         }
         __syncthreads();
         // T = (I + A)^-1, A strictly lower: blocked by 16.  Diagonal blocks by forward
@@ -199,11 +200,6 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
             }
             for (int i = 0; i < BB; ++i)  // zero the block row's entries right of the diagonal
                 for (int jb = blk + 1; jb < NB; ++jb) Tb[(o + i) * (kC + 1) + jb * BB + u] = 0.f;
-        } else {
-            for (int idx = tid - kC; idx < kC * kC; idx += kCT - kC) {
-                const int t = idx / kC, s2 = idx - t * kC;
-                umma::store_split(img + kTBytes, t, s2, kC, Pb[t * (kC + 1) + s2]);
-            }
         }
         __syncthreads();
         // scratch [NB-1][16][16] in the T half of the image buffer, which is written last
@@ -486,7 +482,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 }
 
 constexpr size_t kChainSmem = 2 * kKTokBytes + 2 * kTPBytes + kNS * 2 * kDK * 2 + 3 * (kNS * 2 * kC * 2) + kC * kNS * 4;
-constexpr size_t kPrepSmem = kKQBytes + 3 * kC * (kC + 1) * 4 + kTPBytes;
+constexpr size_t kPrepSmem = (4 * kC * (kC + 1) * 4 + kTPBytes) > kKQBytes ? (4 * kC * (kC + 1) * 4 + kTPBytes) : kKQBytes;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 

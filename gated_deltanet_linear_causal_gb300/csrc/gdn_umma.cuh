@@ -57,22 +57,21 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
 }
 
 // D (+)= A * B^T over K logical columns, both operands split (ktot = 2K) and K-major;
-// A has M rows, B has N rows.  Issued by one thread.
+// A has M rows, B has N rows.  Issued by one thread: the descriptors are formed
+// once and advanced by adding the byte offset / 16 to their address field.
 __device__ __forceinline__ void mma_split_kk(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
                                              int N, int K, bool accumulate) {
     const uint32_t idesc = idesc_bf16(M, N);
     const uint32_t sbo = (uint32_t)(2 * K / 8) * 128;
-    const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+    const uint64_t da = smem_desc(smem_u32(a), 128, sbo), db = smem_desc(smem_u32(b), 128, sbo);
+    const uint64_t lo = (uint64_t)(K / 8) * 128 / 16;  // descriptor step to the lo half
     bool acc = accumulate;
-#pragma unroll
-    for (int pr = 0; pr < 3; ++pr) {  // (hi, hi), (hi, lo), (lo, hi)
-        const int pa = pr == 2, pb = pr == 1;
-        for (int ks = 0; ks < K / 16; ++ks) {
-            const uint32_t ka = (uint32_t)((pa * K + 16 * ks) / 8) * 128;
-            const uint32_t kb = (uint32_t)((pb * K + 16 * ks) / 8) * 128;
-            mma_bf16(d_tmem, smem_desc(sa + ka, 128, sbo), smem_desc(sb + kb, 128, sbo), idesc, acc);
-            acc = true;
-        }
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t step = (uint64_t)(2 * ks) * 128 / 16;  // 16 columns = 2 core matrices
+        mma_bf16(d_tmem, da + step, db + step, idesc, acc);            // hi * hi
+        mma_bf16(d_tmem, da + step, db + step + lo, idesc, true);      // hi * lo
+        mma_bf16(d_tmem, da + step + lo, db + step, idesc, true);      // lo * hi
+        acc = true;
     }
 }
 
@@ -83,17 +82,15 @@ __device__ __forceinline__ void mma_split_mn(uint32_t d_tmem, const unsigned cha
     const uint32_t idesc = idesc_bf16(M, N, true);
     const uint32_t a_kstep = (uint32_t)(2 * M / 8) * 128;  // next 8 rows of the stored A (= next 8 along K)
     const uint32_t b_sbo = (uint32_t)(2 * Kdim / 8) * 128;
-    const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+    const uint64_t da = smem_desc(smem_u32(a), a_kstep, 128), db = smem_desc(smem_u32(b), 128, b_sbo);
+    const uint64_t alo = (uint64_t)(M / 8) * 128 / 16, blo = (uint64_t)(Kdim / 8) * 128 / 16;
     bool acc = accumulate;
-#pragma unroll
-    for (int pr = 0; pr < 3; ++pr) {
-        const int pa = pr == 2, pb = pr == 1;
-        for (int ks = 0; ks < Kdim / 16; ++ks) {
-            const uint32_t oa = (uint32_t)(2 * ks) * a_kstep + (uint32_t)(pa * M / 8) * 128;
-            const uint32_t ob = (uint32_t)((pb * Kdim + 16 * ks) / 8) * 128;
-            mma_bf16(d_tmem, smem_desc(sa + oa, a_kstep, 128), smem_desc(sb + ob, 128, b_sbo), idesc, acc);
-            acc = true;
-        }
+    for (int ks = 0; ks < Kdim / 16; ++ks) {
+        const uint64_t sa = (uint64_t)(2 * ks) * a_kstep / 16, sb = (uint64_t)(2 * ks) * 128 / 16;
+        mma_bf16(d_tmem, da + sa, db + sb, idesc, acc);
+        mma_bf16(d_tmem, da + sa, db + sb + blo, idesc, true);
+        mma_bf16(d_tmem, da + sa + alo, db + sb, idesc, true);
+        acc = true;
     }
 }
 
