@@ -253,10 +253,12 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     unsigned char* ktok = smem;                        // 32 KB  K   [64 tok][2*128]
     unsigned char* qtok = ktok + kKTokBytes;           // 32 KB  Q   [64 tok][2*128]
     unsigned char* tpb = qtok + kKTokBytes;            // 2 x 32 KB  T, P [64][2*64]
-    unsigned char* s0t = tpb + 2 * kTPBytes;           // 16 KB  S0^T [32 cols][2*128]
-    unsigned char* rt = s0t + kNS * 2 * kDK * 2;       //  8 KB  R^T  [32][2*64]
-    unsigned char* ut = rt + kNS * 2 * kC * 2;         //  8 KB  U^T
-    unsigned char* cut = ut + kNS * 2 * kC * 2;        //  8 KB  (diag(c) U)^T
+    // B operands stored MN-major (rows along K, each thread writes its own row as
+    // 16-byte vectors): S0 [128 key rows][2*32], R, U, diag(c) U [64 tokens][2*32]
+    unsigned char* s0t = tpb + 2 * kTPBytes;           // 16 KB  S0
+    unsigned char* rt = s0t + kNS * 2 * kDK * 2;       //  8 KB  R
+    unsigned char* ut = rt + kNS * 2 * kC * 2;         //  8 KB  U
+    unsigned char* cut = ut + kNS * 2 * kC * 2;        //  8 KB  diag(c) U
     float* vv = reinterpret_cast<float*>(cut + kNS * 2 * kC * 2);  // [64][32]
     __shared__ float s_g[kC], s_b[kC], s_G[kC], s_carry;
     __shared__ uint32_t s_tmem;
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
     }
 #pragma unroll
-    for (int j = 0; j < kNS; ++j) umma::store_split(s0t, j, tid, kDK, S[j]);
+    for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
 
     if (warp == 0) umma::tmem_alloc(&s_tmem, 256);
     if (tid == 0) {
@@ -381,8 +383,8 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         if (s_abort) break;
         umma::fence_after_sync();
         if (tid == 0) {
-            umma::mma_split_kk(tDk, ktok, s0t, kC, kNS, kDK, false);
-            umma::mma_split_kk(tDq, qtok, s0t, kC, kNS, kDK, false);
+            umma::mma_split(tDk, ktok, false, s0t, true, kC, kNS, kDK, false);
+            umma::mma_split(tDq, qtok, false, s0t, true, kC, kNS, kDK, false);
             umma::commit(&s_mma);
             ++mma_iss;
         }
@@ -395,9 +397,11 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         const float gam_t = expf(s_G[trow]);
         if (lane < 16) {
             const float b = s_b[trow];
+            float rr[kNS];
 #pragma unroll
-            for (int j = 0; j < kNS; ++j)
-                umma::store_split(rt, j, trow, kC, __fmul_rn(b, fmaf(-gam_t, dk[j], vv[trow * kNS + j])));
+            for (int j = 0; j < kNS; ++j) rr[j] = __fmul_rn(b, fmaf(-gam_t, dk[j], vv[trow * kNS + j]));
+#pragma unroll
+            for (int j = 0; j < kNS; j += 8) umma::store_split8(rt, trow, j, kNS, rr + j);
         }
         fence_proxy_async_smem();
         umma::fence_before_sync();
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 
         // ---- round 2: U = T R ----
         if (tid == 0) {
-            umma::mma_split_kk(tU, tpi, rt, kC, kNS, kC, false);
+            umma::mma_split(tU, tpi, false, rt, true, kC, kNS, kC, false);
             umma::commit(&s_mma);
             ++mma_iss;
         }
@@ -417,10 +421,13 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         umma::tmem_ld32(tU + wl, uu);
         if (lane < 16) {
             const float cdec = expf(s_G[kC - 1] - s_G[trow]);
+            float cu[kNS];
 #pragma unroll
-            for (int j = 0; j < kNS; ++j) {
-                umma::store_split(ut, j, trow, kC, uu[j]);
-                umma::store_split(cut, j, trow, kC, __fmul_rn(cdec, uu[j]));
+            for (int j = 0; j < kNS; ++j) cu[j] = __fmul_rn(cdec, uu[j]);
+#pragma unroll
+            for (int j = 0; j < kNS; j += 8) {
+                umma::store_split8(ut, trow, j, kNS, uu + j);
+                umma::store_split8(cut, trow, j, kNS, cu + j);
             }
         }
         fence_proxy_async_smem();
@@ -431,8 +438,8 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 
         // ---- round 3: O = diag(gamma) Q S0 + P U;  S += K^T diag(c) U ----
         if (tid == 0) {
-            umma::mma_split_kk(tO, tpi + kTBytes, ut, kC, kNS, kC, false);
-            umma::mma_split_mn(tS, ktok, cut, kDK, kNS, kC, false);
+            umma::mma_split(tO, tpi + kTBytes, false, ut, true, kC, kNS, kC, false);
+            umma::mma_split(tS, ktok, true, cut, true, kDK, kNS, kC, false);
             umma::commit(&s_mma);
             ++mma_iss;
         }
@@ -454,10 +461,9 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         }
         const float gl = expf(s_G[kC - 1]);
 #pragma unroll
-        for (int j = 0; j < kNS; ++j) {
-            S[j] = fmaf(gl, S[j], ss[j]);
-            umma::store_split(s0t, j, tid, kDK, S[j]);
-        }
+        for (int j = 0; j < kNS; ++j) S[j] = fmaf(gl, S[j], ss[j]);
+#pragma unroll
+        for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
         umma::fence_before_sync();
         __syncthreads();  // this chunk's operand reads are complete
         if (s_abort) break;

@@ -130,10 +130,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrefillArgs a,
         s_fac[tid] = 1.f;
     }
     __syncthreads();
-    for (int idx = tid; idx < nch * kPrepTokens; idx += kPrepThreads) {
-        const int tl = idx / nch, cl = idx - tl * nch;
+    // nch is a power of two (dk or 32): rows of 4 channels go out as 16-byte stores
+    const int lg4 = __ffs(nch / 4) - 1;
+    for (int idx = tid; idx < (nch / 4) * kPrepTokens; idx += kPrepThreads) {
+        const int tl = idx >> lg4, c4 = idx & (nch / 4 - 1);
         const int t = t0 + tl;
-        if (t < a.T) y[(size_t)t * g.D + cbase + cl] = __fmul_rn(tile[cl * (kPrepTokens + 1) + tl], s_fac[tl]);
+        if (t < a.T) {
+            const float f = s_fac[tl];
+            const float* col = tile + 4 * c4 * (kPrepTokens + 1) + tl;
+            const float4 v = make_float4(__fmul_rn(col[0], f), __fmul_rn(col[kPrepTokens + 1], f),
+                                         __fmul_rn(col[2 * (kPrepTokens + 1)], f),
+                                         __fmul_rn(col[3 * (kPrepTokens + 1)], f));
+            *reinterpret_cast<float4*>(y + (size_t)t * g.D + cbase + 4 * c4) = v;
+        }
     }
 }
 

@@ -56,42 +56,52 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         : "memory");
 }
 
-// D (+)= A * B^T over K logical columns, both operands split (ktot = 2K) and K-major;
-// A has M rows, B has N rows.  Issued by one thread: the descriptors are formed
-// once and advanced by adding the byte offset / 16 to their address field.
-__device__ __forceinline__ void mma_split_kk(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
-                                             int N, int K, bool accumulate) {
-    const uint32_t idesc = idesc_bf16(M, N);
-    const uint32_t sbo = (uint32_t)(2 * K / 8) * 128;
-    const uint64_t da = smem_desc(smem_u32(a), 128, sbo), db = smem_desc(smem_u32(b), 128, sbo);
-    const uint64_t lo = (uint64_t)(K / 8) * 128 / 16;  // descriptor step to the lo half
+// D (+)= op(A) op(B) over K logical columns; A gives M rows, B gives N columns.
+// A K-major operand is stored [M (or N) rows][2K]; an MN-major one is stored
+// [K rows][2M (or 2N)], i.e. the same canonical layout read transposed (its
+// leading-dimension offset then steps along K and its stride offset along M/N).
+// Issued by one thread: descriptors are formed once and advanced by adding
+// byte offsets / 16 to their address field.
+__device__ __forceinline__ void mma_split(uint32_t d_tmem, const unsigned char* a, bool a_mn, const unsigned char* b,
+                                          bool b_mn, int M, int N, int K, bool accumulate) {
+    const uint32_t idesc = idesc_bf16(M, N, a_mn) | (b_mn ? (1u << 16) : 0u);
+    const uint32_t a_row = (uint32_t)(2 * M / 8) * 128, b_row = (uint32_t)(2 * N / 8) * 128;
+    const uint32_t k_row = (uint32_t)(2 * K / 8) * 128;
+    const uint64_t da = a_mn ? smem_desc(smem_u32(a), a_row, 128) : smem_desc(smem_u32(a), 128, k_row);
+    const uint64_t db = b_mn ? smem_desc(smem_u32(b), b_row, 128) : smem_desc(smem_u32(b), 128, k_row);
+    const uint64_t a_step = (a_mn ? 2 * a_row : 256) / 16, b_step = (b_mn ? 2 * b_row : 256) / 16;  // 16 along K
+    const uint64_t a_lo = (uint64_t)((a_mn ? M : K) / 8) * 128 / 16, b_lo = (uint64_t)((b_mn ? N : K) / 8) * 128 / 16;
     bool acc = accumulate;
     for (int ks = 0; ks < K / 16; ++ks) {
-        const uint64_t step = (uint64_t)(2 * ks) * 128 / 16;  // 16 columns = 2 core matrices
-        mma_bf16(d_tmem, da + step, db + step, idesc, acc);            // hi * hi
-        mma_bf16(d_tmem, da + step, db + step + lo, idesc, true);      // hi * lo
-        mma_bf16(d_tmem, da + step + lo, db + step, idesc, true);      // lo * hi
+        const uint64_t ka = da + ks * a_step, kb = db + ks * b_step;
+        mma_bf16(d_tmem, ka, kb, idesc, acc);            // hi * hi
+        mma_bf16(d_tmem, ka, kb + b_lo, idesc, true);    // hi * lo
+        mma_bf16(d_tmem, ka + a_lo, kb, idesc, true);    // lo * hi
         acc = true;
     }
 }
 
-// D (+)= A^T * B^T where A is stored K-major as [Kdim rows][M columns] split over
-// its columns (ktot_a = 2M) and read MN-major; B is K-major [N rows][2*Kdim].
-__device__ __forceinline__ void mma_split_mn(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
-                                             int N, int Kdim, bool accumulate) {
-    const uint32_t idesc = idesc_bf16(M, N, true);
-    const uint32_t a_kstep = (uint32_t)(2 * M / 8) * 128;  // next 8 rows of the stored A (= next 8 along K)
-    const uint32_t b_sbo = (uint32_t)(2 * Kdim / 8) * 128;
-    const uint64_t da = smem_desc(smem_u32(a), a_kstep, 128), db = smem_desc(smem_u32(b), 128, b_sbo);
-    const uint64_t alo = (uint64_t)(M / 8) * 128 / 16, blo = (uint64_t)(Kdim / 8) * 128 / 16;
-    bool acc = accumulate;
-    for (int ks = 0; ks < Kdim / 16; ++ks) {
-        const uint64_t sa = (uint64_t)(2 * ks) * a_kstep / 16, sb = (uint64_t)(2 * ks) * 128 / 16;
-        mma_bf16(d_tmem, da + sa, db + sb, idesc, acc);
-        mma_bf16(d_tmem, da + sa, db + sb + blo, idesc, true);
-        mma_bf16(d_tmem, da + sa + alo, db + sb, idesc, true);
-        acc = true;
+// Both operands K-major: D (+)= A B^T with A [M][2K], B [N][2K].
+__device__ __forceinline__ void mma_split_kk(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
+                                             int N, int K, bool accumulate) {
+    mma_split(d_tmem, a, false, b, false, M, N, K, accumulate);
+}
+
+// Store 8 consecutive fp32 values as the hi and lo halves of row r, columns
+// c0..c0+7 (c0 % 8 == 0) of a split operand image with N logical columns:
+// two 16-byte stores.
+__device__ __forceinline__ void store_split8(unsigned char* base, int r, int c0, int N, const float* v) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        const float2 hf = __bfloat1622float2(h2);
+        const __nv_bfloat162 l2 = __floats2bfloat162_rn(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
+        hi[j] = *reinterpret_cast<const uint32_t*>(&h2);
+        lo[j] = *reinterpret_cast<const uint32_t*>(&l2);
     }
+    *reinterpret_cast<uint4*>(base + kmajor_offset(r, c0, 2 * N)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(base + kmajor_offset(r, N + c0, 2 * N)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
 __device__ __forceinline__ void commit(uint64_t* bar) {
