@@ -111,16 +111,19 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
     const int cnt = min(kC, a.cu[n + 1] - t0);
 
     // K and Q of the chunk as split operand images [token][dk]
-    for (int idx = tid; idx < kC * kDK; idx += kCT) {
-        const int t = idx / kDK, i = idx - t * kDK;
-        float kv = 0.f, qv = 0.f;
+    for (int idx = tid; idx < kC * kDK / 8; idx += kCT) {  // 8 consecutive key dims per step
+        const int t = idx / (kDK / 8), i0 = 8 * (idx - t * (kDK / 8));
+        float kv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (t < cnt) {
             const float* row = y + (size_t)(t0 + t) * g.D;
-            kv = row[g.Hk * kDK + hk * kDK + i];
-            qv = row[hk * kDK + i];
+            const float4* kr = reinterpret_cast<const float4*>(row + g.Hk * kDK + hk * kDK + i0);
+            const float4* qr = reinterpret_cast<const float4*>(row + hk * kDK + i0);
+            const float4 k0 = kr[0], k1 = kr[1], q0 = qr[0], q1 = qr[1];
+            kv[0] = k0.x; kv[1] = k0.y; kv[2] = k0.z; kv[3] = k0.w; kv[4] = k1.x; kv[5] = k1.y; kv[6] = k1.z; kv[7] = k1.w;
+            qv[0] = q0.x; qv[1] = q0.y; qv[2] = q0.z; qv[3] = q0.w; qv[4] = q1.x; qv[5] = q1.y; qv[6] = q1.z; qv[7] = q1.w;
         }
-        umma::store_split(ktok, t, i, kDK, kv);
-        umma::store_split(qtok, t, i, kDK, qv);
+        umma::store_split8(ktok, t, i0, kDK, kv);
+        umma::store_split8(qtok, t, i0, kDK, qv);
     }
     if (warp == 0) umma::tmem_alloc(&s_tmem, 128);
     if (tid == 0) {
@@ -176,11 +179,17 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
         }
         __syncthreads();
         scan64(s_g, s_G, &s_carry);
-        for (int idx = tid; idx < kC * kC; idx += kCT) {
-            const int t = idx / kC, s = idx - t * kC;
-            const float dec = s <= t ? expf(s_G[t] - s_G[s]) : 0.f;
-            Ab[t * (kC + 1) + s] = s < t ? __fmul_rn(__fmul_rn(s_b[t], dec), kk[t * (kC + 1) + s]) : 0.f;
-            umma::store_split(img + kTBytes, t, s, kC, __fmul_rn(dec, qk[t * (kC + 1) + s]));  // P
+        for (int idx = tid; idx < kC * kC / 8; idx += kCT) {  // 8 consecutive s per step
+            const int t = idx / (kC / 8), s0 = 8 * (idx - t * (kC / 8));
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int s = s0 + e;
+                const float dec = s <= t ? expf(s_G[t] - s_G[s]) : 0.f;
+                Ab[t * (kC + 1) + s] = s < t ? __fmul_rn(__fmul_rn(s_b[t], dec), kk[t * (kC + 1) + s]) : 0.f;
+                pv[e] = __fmul_rn(dec, qk[t * (kC + 1) + s]);
+            }
+            umma::store_split8(img + kTBytes, t, s0, kC, pv);  // P
         }
         __syncthreads();
         // T = (I + A)^-1, A strictly lower: blocked by 16.  Diagonal blocks by forward
@@ -227,9 +236,12 @@ __global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a,
             }
             __syncthreads();
         }
-        for (int idx = tid; idx < kC * kC; idx += kCT) {
-            const int t = idx / kC, s = idx - t * kC;
-            umma::store_split(img, t, s, kC, Tb[t * (kC + 1) + s]);
+        for (int idx = tid; idx < kC * kC / 8; idx += kCT) {
+            const int t = idx / (kC / 8), s0 = 8 * (idx - t * (kC / 8));
+            float tv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tv[e] = Tb[t * (kC + 1) + s0 + e];
+            umma::store_split8(img, t, s0, kC, tv);
         }
         __syncthreads();
         const uint4* src = reinterpret_cast<const uint4*>(img);
