@@ -4,23 +4,29 @@
 // Step 5 of the MNN "Qwen3.5" page (section 1.2) over a chunk of C tokens that
 // starts from state S0.  With G_t the running sum of the chunk's log-decays,
 // gamma_t = exp(G_t) and c_t = exp(G_last - G_t), unrolling the recurrence gives
-//   U     = T R,  R = diag(beta) (V - diag(gamma) K S0),
+//   U     = u - W S0,  u = T diag(beta) V,  W = T diag(beta gamma) K,
 //   T     = (I + A)^-1,  A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s) for s < t,
-//   O     = diag(gamma) Q S0 + P U,  P[t][s] = e^{G_t-G_s} (q_t.k_s) for s <= t,
-//   S_end = gamma_last S0 + K^T diag(c) U,
-// where row t of U is the token's delta (beta_t (v_t - v_pred)).  T and P do
-// not depend on S0, so:
-//   chunk_prep_kernel  (every chunk x key head in parallel) forms the Gram
-//       matrices K K^T and Q K^T on the tensor cores, then T and P for each value
-//       head of the key head, and writes them, with the chunk's K and Q, as
-//       tensor-core operand images to the workspace;
+//   O     = Q~ S0 + P U,  Q~ = diag(gamma) Q,  P[t][s] = e^{G_t-G_s} (q_t.k_s) for s <= t,
+//   S_end = gamma_last S0 + K~^T U,  K~ = diag(c) K,
+// where row t of U is the token's delta (beta_t (v_t - v_pred)).  Only the
+// products with S0 depend on the previous chunk, so:
+//   chunk_prep_kernel  (every chunk x key head in parallel) runs steps 1-4 on
+//       the chunk's raw qkv columns (the conv window reaching back into the
+//       previous chunk or the carried conv state), forms K K^T and Q K^T on the
+//       tensor cores, then for each value head of the key head T, and W and u
+//       as tensor-core products, and writes W, Q~, K~, P (as operand images) and
+//       u to the workspace;
 //   chain_kernel  (one CTA per sequence x value head x 32 value columns) walks
-//       the chunks in order, three tensor-core rounds per chunk:
-//         [K S0, Q S0] -> R -> [T R] -> U -> [P U, K^T diag(c) U] -> O, S_end.
+//       the chunks in order, two dependent tensor-core rounds per chunk:
+//         [W S0, Q~ S0] -> U = u - W S0 -> [K~^T U, P U] -> S_end,
+//       and reads O = Q~ S0 + P U out of tensor memory while the next chunk's
+//       first round runs.
 // Every product takes fp32 operands as bf16 hi/lo pairs and accumulates
 // hi*hi + hi*lo + lo*hi in fp32 (gdn_umma.cuh): a single bf16 or tf32 pass
 // misses the output and state tolerances on this recurrence.
-// The path covers head_k_dim = 128 and head_v_dim a multiple of 32.
+// The path covers head_k_dim = 128, head_v_dim in {32, 64, 96, 128}, conv
+// width <= 4 and up to 16 value heads per key head.
+
 #include <algorithm>
 
 #include "gdn_common.cuh"
@@ -34,14 +40,26 @@ static __device__ int32_t g_chunk_error;  // set to GDN_ERR_DEVICE_TIMEOUT (7) b
 
 namespace {
 
-constexpr int kC = 64;     // chunk length
-constexpr int kDK = 128;   // head_k_dim handled here
-constexpr int kNS = 32;    // value columns per chain CTA
-constexpr int kCT = 128;   // threads per CTA
-constexpr uint32_t kKTokBytes = kC * 2 * kDK * 2;       // one split [64 tokens][2*128] image: 32 KB
-constexpr uint32_t kKQBytes = 2 * kKTokBytes;           // K and Q images of a (chunk, key head)
-constexpr uint32_t kTBytes = kC * 2 * kC * 2;           // one split [64][2*64] image: 16 KB
-constexpr uint32_t kTPBytes = 2 * kTBytes;              // T and P images of a (chunk, value head)
+constexpr int kC = 64;      // chunk length
+constexpr int kDK = 128;    // head_k_dim handled here
+constexpr int kNS = 32;     // value columns per chain CTA
+constexpr int kMaxDV = 128;  // widest head_v_dim handled here
+constexpr int kKC = 4;      // widest conv handled here
+constexpr int kMaxF = 16;   // value heads per key head
+constexpr int kPT = 512;    // chunk-prep threads
+constexpr int kCT = 128;    // chain threads
+constexpr uint32_t kImgBytes = kC * 2 * kDK * 2;  // split [64 tokens][2*128] image: 32 KB
+constexpr uint32_t kPBytes = kC * 2 * kC * 2;     // split [64][2*64] image: 16 KB
+constexpr uint32_t kWQBytes = 2 * kImgBytes;      // W and Q~ of a (chunk, value head)
+constexpr uint32_t kKPBytes = kImgBytes + kPBytes;  // K~ and P of a (chunk, value head)
+constexpr uint32_t kUSlice = kC * kNS * 4;        // fp32 u rows of one chain CTA: 8 KB
+// raw-input row: 128 channels + pad; 16-byte rows that start 4 banks apart
+template <typename T>
+struct RawW {
+    static constexpr int value = sizeof(T) == 2 ? kMaxDV + 8 : kMaxDV + 4;
+};
+constexpr int kLd = kC + 1;                       // padded fp32 [64][65] matrices
+constexpr int kAld = kC + 4;                      // fp32 [64][68] A: 16-byte rows
 
 // Chunk offsets: coff[n] = number of chunks of the sequences before n.
 __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int32_t* __restrict__ coff) {
@@ -66,219 +84,440 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* coff, int N, int chun
     return lo;
 }
 
-// Inclusive prefix sum of g[0..63] in shared memory by warps 0 and 1 (the others
-// pass through); result in G[0..63].
-__device__ __forceinline__ void scan64(const float* g, float* G, float* carry) {
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (tid < 64) {
-        float v = g[tid];
+// Inclusive prefix sums of the log-decays of the f value heads, G[j][0..63] in
+// place: warps 2i and 2i+1 scan the two halves of head j = i (+4 per pass).
+__device__ __forceinline__ void scan_heads(float* G, int f) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j0 = 0; j0 < f; j0 += kPT / 64) {
+        const int j = j0 + (warp >> 1);
+        if (j < f) {
+            float v = G[j * kC + 32 * (warp & 1) + lane];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) v += o;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += o;
+            }
+            G[j * kC + 32 * (warp & 1) + lane] = v;
         }
-        if (tid == 31) *carry = v;
-        G[tid] = v;
+        __syncthreads();
+        if (j < f && (warp & 1)) G[j * kC + 32 + lane] += G[j * kC + 31];
+        __syncthreads();
     }
-    __syncthreads();
-    if (tid >= 32 && tid < 64) G[tid] += *carry;
-    __syncthreads();
 }
 
-// ---- chunk prep ----------------------------------------------------------------
+// Shared-memory carve-up of chunk_prep_kernel (byte offsets).  Raw inputs are
+// held for 128 channels at a time in rows of RawW elements.
 template <typename T>
-__global__ void __launch_bounds__(kCT, 1) chunk_prep_kernel(const PrefillArgs a, const float* __restrict__ y,
-                                                            const int32_t* __restrict__ coff,
-                                                            unsigned char* __restrict__ kq,
-                                                            unsigned char* __restrict__ tp) {
+struct PrepSmem {
+    static constexpr size_t kimg = 0;                              // K image; Q image right after it
+    static constexpr size_t qimg = kimg + kImgBytes;               // Q image, then each head's V image
+    static constexpr size_t timg = qimg + kImgBytes;               // T diag(beta gamma), T diag(beta)
+    static constexpr size_t kk = timg + 2 * kPBytes;               // fp32 K K^T [64][65]
+    static constexpr size_t qk = kk + kC * kLd * 4;                // fp32 Q K^T [64][65]
+    static constexpr size_t ab = qk + kC * kLd * 4;                // fp32 A [64][68]
+    static constexpr size_t tb = ab + kC * kAld * 4;               // fp32 T [64][65]
+    static constexpr size_t raw = tb + kC * kLd * 4;               // raw inputs [64+K-1][RawW]
+    static constexpr size_t raw_bytes = ((size_t)(kC + kKC - 1) * RawW<T>::value * sizeof(T) + 15) & ~(size_t)15;
+    static constexpr size_t wv = raw + raw_bytes;                  // fp32 conv weights [128][kKC]
+    static constexpr size_t nrm = wv + kMaxDV * kKC * 4;           // fp32 partial sums of squares [8][64]
+    static constexpr size_t gates = nrm + 8 * kC * 4;              // fp32 G, gamma, c, beta [f][64] each
+    static size_t total(int f) { return gates + (size_t)4 * f * kC * 4; }
+};
+
+// ---- chunk prep ----------------------------------------------------------------
+// Workspace records per (chunk, value head): wq = [W image | Q~ image],
+// kp = [K~ image | P image], u = dv/32 slices of fp32 [64][32], gl = gamma_last.
+struct ChunkOut {
+    unsigned char* wq;
+    unsigned char* kp;
+    float* u;
+    float* gl;
+};
+
+// SiLU with the fast exponential and reciprocal: the chunked form is checked
+// against the oracle's tolerance, not bit for bit against the decode path.
+__device__ __forceinline__ float silu_fast(float y) { return __fmul_rn(y, __frcp_rn(__fadd_rn(1.f, __expf(-y)))); }
+
+// Raw inputs of channels chan(i), i < nch, at positions t0-(K-1) .. t0+63 into
+// raw[r][i] (r = position - t0 + K-1): from qkv inside the sequence, from the
+// carried conv state before its start, 0 past the chunk's last token.  Warps
+// w0 .. w0+nw-1, one channel row per warp (lanes along positions, coalesced),
+// kU rows in flight.
+template <typename T, int kU, typename Chan>
+__device__ __forceinline__ void load_raw(const PrefillArgs& a, T* raw, int nch, Chan chan, int n, int tb, int t0,
+                                         int cnt, int w0, int nw) {
+    constexpr int W = RawW<T>::value;
+    const Geom& g = a.g;
+    const int K = g.K, warp = (threadIdx.x >> 5) - w0, lane = threadIdx.x & 31;
+    const T* qkv = static_cast<const T*>(a.qkv);
+    const T* cst = static_cast<const T*>(a.conv_state);
+    constexpr int kRows = (kC + kKC - 1 + 31) / 32;
+    for (int i0 = kU * warp; i0 < nch; i0 += kU * nw) {
+        T v[kU][kRows];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u;
+            const int c = i < nch ? chan(i) : 0;
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) {
+                const int r = lane + 32 * q, j = r - (K - 1), p = t0 + j;
+                v[u][q] = zero_elem<T>();
+                if (i < nch && r < kC + K - 1 && j < cnt)
+                    v[u][q] = p >= tb ? qkv[(size_t)c * a.T + p] : cst[((size_t)n * g.D + c) * (K - 1) + (p - tb + K - 1)];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) {
+                const int r = lane + 32 * q;
+                if (i0 + u < nch && r < kC + K - 1) raw[r * W + i0 + u] = v[u][q];
+            }
+    }
+}
+
+// Eight consecutive channels c..c+7 of raw row r as fp32.
+__device__ __forceinline__ void raw8(const __nv_bfloat16* raw, int r, int c, float (&x)[8]) {
+    const uint4 b = *reinterpret_cast<const uint4*>(raw + r * RawW<__nv_bfloat16>::value + c);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void raw8(const float* raw, int r, int c, float (&x)[8]) {
+    const float4 lo = *reinterpret_cast<const float4*>(raw + r * RawW<float>::value + c);
+    const float4 hi = *reinterpret_cast<const float4*>(raw + r * RawW<float>::value + c + 4);
+    x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+    x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+}
+
+// Depthwise causal conv + SiLU of channels c..c+7 at chunk token t (raw rows
+// t .. t+K-1, newest last); weights wv[channel][kKC].
+template <typename T>
+__device__ __forceinline__ void conv8(const T* raw, const float* wv, int t, int c, int K, float (&y)[8]) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float4 wt[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) wt[e] = *reinterpret_cast<const float4*>(wv + (c + e) * kKC);
+#pragma unroll
+    for (int tap = 0; tap < kKC; ++tap)
+        if (tap < K) {
+            float x[8];
+            raw8(raw, t + tap, c, x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float wk = tap == 0 ? wt[e].x : tap == 1 ? wt[e].y : tap == 2 ? wt[e].z : wt[e].w;
+                acc[e] = fmaf(wk, x[e], acc[e]);
+            }
+        }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y[e] = silu_fast(acc[e]);
+}
+
+// T = (I + A)^-1 for strictly lower A (row stride kAld): column u (one thread per
+// column) by forward substitution, T[i][u] = -sum_{s<i} A[i][s] T[s][u] for
+// i > u, T[u][u] = 1, four rows at a time (each T[s][u] read once per block, A
+// rows as broadcast float4 reads), into Tb (row stride kLd).
+__device__ __forceinline__ void inverse_column(const float* A, float* Tb, int u) {
+    for (int ib = 0; ib < kC; ib += 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+        for (int s = 0; s < ib; s += 4) {
+            const float t0 = Tb[(s + 0) * kLd + u], t1 = Tb[(s + 1) * kLd + u];
+            const float t2 = Tb[(s + 2) * kLd + u], t3 = Tb[(s + 3) * kLd + u];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float4 a4 = *reinterpret_cast<const float4*>(A + (ib + r) * kAld + s);
+                acc[r] = fmaf(a4.x, t0, fmaf(a4.y, t1, fmaf(a4.z, t2, fmaf(a4.w, t3, acc[r]))));
+            }
+        }
+        float tv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = ib + r;
+            float sum = acc[r];
+#pragma unroll
+            for (int q = 0; q < r; ++q) sum = fmaf(A[i * kAld + ib + q], tv[q], sum);
+            tv[r] = i < u ? 0.f : i == u ? 1.f : -sum;
+            Tb[i * kLd + u] = tv[r];
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a, const int32_t* __restrict__ coff,
+                                                            const ChunkOut ws) {
+    using L = PrepSmem<T>;
     extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char* ktok = smem;                                         // 32 KB
-    unsigned char* qtok = smem + kKTokBytes;                            // 32 KB
-    float* kk = reinterpret_cast<float*>(smem);                         // [64][65], after the MMAs
-    float* qk = kk + kC * (kC + 1);                                     // [64][65]
-    // after the MMAs: kk, qk [64][65] over the images, then A and T [64][65] and the
-    // T and P operand images (32 KB)
-    float* Ab = qk + kC * (kC + 1);
-    float* Tb = Ab + kC * (kC + 1);
-    unsigned char* img = reinterpret_cast<unsigned char*>(Tb + kC * (kC + 1));
-    __shared__ float s_g[kC], s_b[kC], s_G[kC], s_carry;
+    unsigned char* kimg = smem + L::kimg;
+    unsigned char* qimg = smem + L::qimg;  // the V image of each value head after the Gram products
+    unsigned char* timg = smem + L::timg;
+    float* kk = reinterpret_cast<float*>(smem + L::kk);
+    float* qk = reinterpret_cast<float*>(smem + L::qk);
+    float* Ab = reinterpret_cast<float*>(smem + L::ab);
+    float* Tb = reinterpret_cast<float*>(smem + L::tb);
+    T* raw = reinterpret_cast<T*>(smem + L::raw);
+    float* wv = reinterpret_cast<float*>(smem + L::wv);
+    float* nrm = reinterpret_cast<float*>(smem + L::nrm);
+    const Geom& g = a.g;
+    const int f = g.f;
+    float* sG = reinterpret_cast<float*>(smem + L::gates);
+    float* sGam = sG + f * kC;
+    float* sCd = sGam + f * kC;
+    float* sBet = sCd + f * kC;
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_bar;
-    const Geom& g = a.g;
+    __shared__ int s_fail;
+
     const int chunk = blockIdx.x, hk = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = seq_of_chunk(coff, a.N, chunk);
-    const int t0 = a.cu[n] + (chunk - coff[n]) * kC;
+    const int tb = a.cu[n];
+    const int t0 = tb + (chunk - coff[n]) * kC;
     const int cnt = min(kC, a.cu[n + 1] - t0);
-
-    // K and Q of the chunk as split operand images [token][dk]
-    for (int idx = tid; idx < kC * kDK / 8; idx += kCT) {  // 8 consecutive key dims per step
-        const int t = idx / (kDK / 8), i0 = 8 * (idx - t * (kDK / 8));
-        float kv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (t < cnt) {
-            const float* row = y + (size_t)(t0 + t) * g.D;
-            const float4* kr = reinterpret_cast<const float4*>(row + g.Hk * kDK + hk * kDK + i0);
-            const float4* qr = reinterpret_cast<const float4*>(row + hk * kDK + i0);
-            const float4 k0 = kr[0], k1 = kr[1], q0 = qr[0], q1 = qr[1];
-            kv[0] = k0.x; kv[1] = k0.y; kv[2] = k0.z; kv[3] = k0.w; kv[4] = k1.x; kv[5] = k1.y; kv[6] = k1.z; kv[7] = k1.w;
-            qv[0] = q0.x; qv[1] = q0.y; qv[2] = q0.z; qv[3] = q0.w; qv[4] = q1.x; qv[5] = q1.y; qv[6] = q1.z; qv[7] = q1.w;
-        }
-        umma::store_split8(ktok, t, i0, kDK, kv);
-        umma::store_split8(qtok, t, i0, kDK, qv);
-    }
-    if (warp == 0) umma::tmem_alloc(&s_tmem, 128);
+    const int K = g.K;
+    const T* w = static_cast<const T*>(a.w);
+    if (warp == 0) umma::tmem_alloc(&s_tmem, 512);
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         fence_mbar_init();
+        s_fail = 0;
     }
+    // log-decays and betas of the value heads
+    for (int idx = tid; idx < f * kC; idx += kPT) {
+        const int j = idx / kC, t = idx - j * kC;
+        const bool in = t < cnt;
+        sG[idx] = in ? a.gate[(size_t)(t0 + t) * g.Hv + hk * f + j] : 0.f;
+        sBet[idx] = in ? a.beta[(size_t)(t0 + t) * g.Hv + hk * f + j] : 0.f;
+    }
+
+    // ---- steps 1-4 for Q, then K: conv + SiLU, L2 norm (1/sqrt(dk) for Q) ----
+    // thread (t, part): token t = tid % 64, channels 16*part .. +15 of the head;
+    // lanes run along tokens, so operand-image rows are written 16 bytes apart
+    for (int pass = 0; pass < 2; ++pass) {
+        const int cb = pass == 0 ? hk * kDK : g.Hk * kDK + hk * kDK;
+        load_raw<T, 8>(a, raw, kDK, [&](int i) { return cb + i; }, n, tb, t0, cnt, 0, kPT / 32);
+        for (int idx = tid; idx < kDK * kKC; idx += kPT) {
+            const int c = idx / kKC, tap = idx - c * kKC;
+            wv[idx] = tap < K ? to_f32(w[(size_t)(cb + c) * K + tap]) : 0.f;
+        }
+        __syncthreads();
+        if (pass == 0) {
+            scan_heads(sG, f);
+            for (int idx = tid; idx < f * kC; idx += kPT) {
+                const int j = idx / kC;
+                const float G = sG[idx];
+                sGam[idx] = expf(G);
+                sCd[idx] = expf(sG[j * kC + kC - 1] - G);
+            }
+            if (tid < f) ws.gl[(size_t)chunk * g.Hv + hk * f + tid] = expf(sG[tid * kC + kC - 1]);
+        }
+        const int t = tid & (kC - 1), part = tid >> 6;
+        float v[16];
+        float ss = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+            float y[8];
+            conv8(raw, wv, t, 16 * part + 8 * gi, K, y);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[8 * gi + e] = y[e];
+                ss = fmaf(y[e], y[e], ss);
+            }
+        }
+        nrm[part * kC + t] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) tot += nrm[p * kC + t];
+        const float r = g.use_l2 ? rsqrtf(tot + g.eps) : 1.f;
+        const float fac = pass ? r : __fmul_rn(g.q_scale, r);
+        const bool in = t < cnt;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = in ? __fmul_rn(v[e], fac) : 0.f;
+        unsigned char* img = pass ? kimg : qimg;
+        umma::store_split8(img, t, 16 * part, kDK, v);
+        umma::store_split8(img, t, 16 * part + 8, kDK, v + 8);
+        for (int j = 0; j < f; ++j) {  // Q~ = diag(gamma) Q and K~ = diag(c) K of each value head
+            const size_t rec = (size_t)chunk * g.Hv + hk * f + j;
+            const float sc = pass ? sCd[j * kC + t] : sGam[j * kC + t];
+            unsigned char* dst = pass ? ws.kp + rec * kKPBytes : ws.wq + rec * kWQBytes + kImgBytes;
+            float sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = __fmul_rn(sc, v[e]);
+            umma::store_split8(dst, t, 16 * part, kDK, sv);
+            umma::store_split8(dst, t, 16 * part + 8, kDK, sv + 8);
+        }
+        __syncthreads();  // raw inputs, weights and partial sums are reused by the next pass
+    }
+
+    // ---- [K; Q] K^T on the tensor cores: rows 0-63 K K^T, rows 64-127 Q K^T ----
     fence_proxy_async_smem();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = s_tmem;
+    const uint32_t tG = tmem, tW = tmem + 128, tU = tmem + 256;
     if (tid == 0) {
-        umma::mma_split_kk(tmem + 0, ktok, ktok, kC, kC, kDK, false);   // K K^T
-        umma::mma_split_kk(tmem + 64, qtok, ktok, kC, kC, kDK, false);  // Q K^T
+        umma::mma_split(tG, kimg, false, kimg, false, 2 * kC, kC, kDK, false);
         umma::commit(&s_bar);
     }
-    // the operand images go to the workspace for the chain kernel meanwhile
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(smem);
-        uint4* dst = reinterpret_cast<uint4*>(kq + ((size_t)chunk * g.Hk + hk) * kKQBytes);
-        for (int i = tid; i < (int)(kKQBytes / 16); i += kCT) dst[i] = src[i];
-    }
-    const bool ok = !__syncthreads_or(!mbar_wait_bounded(&s_bar, 0));
-    umma::fence_after_sync();
-    float vk[32], vq[32];
-    const int row = 16 * warp + (lane & 15);  // M = 64 layout: lanes 0-15 of each warp
-    for (int half = 0; half < 2; ++half) {
-        umma::tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 0 + 32 * half, vk);
-        umma::tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 64 + 32 * half, vq);
-        __syncthreads();  // everyone is past the MMAs' reads of the images before kk/qk overwrite them
-        if (lane < 16 && ok)
-            for (int j = 0; j < 32; ++j) {
-                kk[row * (kC + 1) + 32 * half + j] = vk[j];
-                qk[row * (kC + 1) + 32 * half + j] = vq[j];
+    uint32_t phase = 0;
+    const uint32_t wl = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
+    const int row = 16 * (warp & 3) + (lane & 15);          // M = 64 rows sit in lanes 0-15 of each quarter
+    constexpr int kBarV = 1, kBarT = 2, kGrp = kPT / 2;     // warps 8-15: V; warps 0-7: A, T
+    for (int j = 0; j < f; ++j) {
+        const int h = hk * f + j;
+        const size_t rec = (size_t)chunk * g.Hv + h;
+        if (warp < 8) {
+            const float* Gj = sG + j * kC;
+            const float* Bj = sBet + j * kC;
+            const float* Yj = sGam + j * kC;
+            if (j == 0) {  // the Gram matrices into shared memory
+                if (!mbar_wait_bounded(&s_bar, 0)) s_fail = 1;
+                umma::fence_after_sync();
+                const int lr = 32 * (warp & 3) + lane;  // M = 128: row = TMEM lane
+                float v[32];
+                umma::tmem_ld32(tG + wl + 32 * (warp >> 2), v);
+                float* dst = lr < kC ? kk + lr * kLd : qk + (lr - kC) * kLd;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) dst[32 * (warp >> 2) + q] = v[q];
+                named_sync(kBarT, kGrp);
             }
+            // A (strictly lower) and P; lanes along t
+            unsigned char* pimg = ws.kp + rec * kKPBytes + kImgBytes;
+            for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
+                const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s = s0 + e;
+                    const float dec = s <= t ? expf(Gj[t] - Gj[s]) : 0.f;
+                    Ab[t * kAld + s] = s < t ? __fmul_rn(__fmul_rn(Bj[t], dec), kk[t * kLd + s]) : 0.f;
+                    pv[e] = __fmul_rn(dec, qk[t * kLd + s]);
+                }
+                umma::store_split8(pimg, t, s0, kC, pv);
+            }
+            named_sync(kBarT, kGrp);
+            if (warp < 2) inverse_column(Ab, Tb, tid);
+            named_sync(kBarT, kGrp);
+            // T diag(beta gamma) and T diag(beta) as A operands
+            for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
+                const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
+                float tg[8], tbt[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int s = s0 + e;
+                    const float tv = Tb[t * kLd + s];
+                    tg[e] = __fmul_rn(tv, __fmul_rn(Bj[s], Yj[s]));
+                    tbt[e] = __fmul_rn(tv, Bj[s]);
+                }
+                umma::store_split8(timg, t, s0, kC, tg);
+                umma::store_split8(timg + kPBytes, t, s0, kC, tbt);
+            }
+        } else {
+            // ---- V: raw inputs, weights, conv + SiLU into the V image ----
+            const int cv = 2 * g.Hk * kDK + h * g.dv;  // first V channel of the head
+            const int vt = tid - kGrp;
+            load_raw<T, 16>(a, raw, g.dv, [&](int i) { return cv + i; }, n, tb, t0, cnt, 8, 8);
+            for (int idx = vt; idx < g.dv * kKC; idx += kGrp) {
+                const int c = idx / kKC, tap = idx - c * kKC;
+                wv[idx] = tap < K ? to_f32(w[(size_t)(cv + c) * K + tap]) : 0.f;
+            }
+            if (j == 0 && !mbar_wait_bounded(&s_bar, 0)) s_fail = 1;  // the Q image is free once the Gram products are done
+            named_sync(kBarV, kGrp);
+            for (int idx = vt; idx < kC * (g.dv / 8); idx += kGrp) {
+                const int t = idx & (kC - 1), c = 8 * (idx >> 6);
+                float y[8];
+                conv8(raw, wv, t, c, K, y);
+                if (t >= cnt)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = 0.f;
+                umma::store_split8(qimg, t, c, g.dv, y);
+            }
+        }
+        if (j == 0 && !s_fail) phase ^= 1;
+        fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+        if (s_fail) break;
+        if (tid == 0) {
+            umma::mma_split(tW, timg, false, kimg, true, kC, kDK, kC, false);             // W = T diag(beta gamma) K
+            umma::mma_split(tU, timg + kPBytes, false, qimg, true, kC, g.dv, kC, false);  // u = T diag(beta) V
+            umma::commit(&s_bar);
+        }
+        const bool done = mbar_wait_bounded(&s_bar, phase);
+        if (!done) s_fail = 1;
+        umma::fence_after_sync();
+        const int cq = warp >> 3;  // column half
+        if ((warp & 4) == 0) {     // warps 0-3, 8-11: W rows as a split operand image, 64 columns each
+            unsigned char* wdst = ws.wq + rec * kWQBytes;
+            for (int c0 = 64 * cq; c0 < 64 * cq + 64; c0 += 32) {
+                float v[32];
+                umma::tmem_ld32(tW + wl + c0, v);
+                if (lane < 16)
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) umma::store_split8(wdst, row, c0 + q, kDK, v + q);
+            }
+        } else {  // warps 4-7, 12-15: u rows, fp32, one [64][32] block per 32-column slice
+            float* udst = ws.u + rec * kC * g.dv;
+            for (int sl = 2 * cq; sl < 2 * cq + 2 && sl < g.dv / kNS; ++sl) {
+                float v[32];
+                umma::tmem_ld32(tU + wl + kNS * sl, v);
+                if (lane < 16)
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(udst + ((size_t)sl * kC + row) * kNS + q) =
+                            make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+            }
+        }
+        if (done) phase ^= 1;
+        umma::fence_before_sync();
+        __syncthreads();  // tensor memory, the V image, raw inputs and the T images are free for the next head
+        umma::fence_after_sync();
+        if (s_fail) break;
     }
-    if (!ok && tid == 0) {
+    if (s_fail && tid == 0) {
         flag_device_error(&g_chunk_error, 7);
-        mbar_wait_bounded(&s_bar, 0);  // give the MMAs a last chance to finish before TMEM is freed
+        mbar_wait_bounded(&s_bar, phase);  // give the MMAs a last chance to land before TMEM is freed
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_free(tmem, 128);
-    if (!ok) return;
-
-    // ---- T and P for each value head of the key head ----
-    for (int hl = 0; hl < g.f; ++hl) {
-        const int h = hk * g.f + hl;
-        if (tid < kC) {
-            const bool in = tid < cnt;
-            s_g[tid] = in ? a.gate[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
-            s_b[tid] = in ? a.beta[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
-        }
-        __syncthreads();
-        scan64(s_g, s_G, &s_carry);
-        for (int idx = tid; idx < kC * kC / 8; idx += kCT) {  // 8 consecutive s per step
-            const int t = idx / (kC / 8), s0 = 8 * (idx - t * (kC / 8));
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int s = s0 + e;
-                const float dec = s <= t ? expf(s_G[t] - s_G[s]) : 0.f;
-                Ab[t * (kC + 1) + s] = s < t ? __fmul_rn(__fmul_rn(s_b[t], dec), kk[t * (kC + 1) + s]) : 0.f;
-                pv[e] = __fmul_rn(dec, qk[t * (kC + 1) + s]);
-            }
-            umma::store_split8(img + kTBytes, t, s0, kC, pv);  // P
-        }
-        __syncthreads();
-        // T = (I + A)^-1, A strictly lower: blocked by 16.  Diagonal blocks by forward
-        // substitution (one thread per column of each block), then the block
-        // sub-diagonals d = 1, 2, 3: T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj.
-        constexpr int BB = 16, NB = kC / BB;
-        if (tid < kC) {
-            const int blk = tid / BB, u = tid % BB, o = blk * BB;
-            for (int i = 0; i < BB; ++i) {
-                float v = i == u ? 1.f : 0.f;
-                if (i > u) {
-                    float acc = 0.f;
-                    for (int s2 = u; s2 < i; ++s2) acc = fmaf(Ab[(o + i) * (kC + 1) + o + s2], Tb[(o + s2) * (kC + 1) + o + u], acc);
-                    v = -acc;
-                }
-                Tb[(o + i) * (kC + 1) + o + u] = v;
-            }
-            for (int i = 0; i < BB; ++i)  // zero the block row's entries right of the diagonal
-                for (int jb = blk + 1; jb < NB; ++jb) Tb[(o + i) * (kC + 1) + jb * BB + u] = 0.f;
-        }
-        __syncthreads();
-        // scratch [NB-1][16][16] in the T half of the image buffer, which is written last
-        float* Xb = reinterpret_cast<float*>(img);
-        for (int d = 1; d < NB; ++d) {
-            const int npair = NB - d;
-            // X_p = sum_{k=j}^{i-1} A_ik T_kj for pair p: (i, j) = (j + d, j), j = p
-            for (int idx = tid; idx < npair * BB * BB; idx += kCT) {
-                const int p = idx / (BB * BB), r = (idx / BB) % BB, cc = idx % BB;
-                const int bi = p + d, bj = p;
-                float acc = 0.f;
-                for (int kb = bj; kb < bi; ++kb)
-                    for (int m = 0; m < BB; ++m)
-                        acc = fmaf(Ab[(bi * BB + r) * (kC + 1) + kb * BB + m], Tb[(kb * BB + m) * (kC + 1) + bj * BB + cc], acc);
-                Xb[idx] = acc;
-            }
-            __syncthreads();
-            for (int idx = tid; idx < npair * BB * BB; idx += kCT) {
-                const int p = idx / (BB * BB), r = (idx / BB) % BB, cc = idx % BB;
-                const int bi = p + d, bj = p;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m)
-                    acc = fmaf(Tb[(bi * BB + r) * (kC + 1) + bi * BB + m], Xb[p * BB * BB + m * BB + cc], acc);
-                Tb[(bi * BB + r) * (kC + 1) + bj * BB + cc] = -acc;
-            }
-            __syncthreads();
-        }
-        for (int idx = tid; idx < kC * kC / 8; idx += kCT) {
-            const int t = idx / (kC / 8), s0 = 8 * (idx - t * (kC / 8));
-            float tv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) tv[e] = Tb[t * (kC + 1) + s0 + e];
-            umma::store_split8(img, t, s0, kC, tv);
-        }
-        __syncthreads();
-        const uint4* src = reinterpret_cast<const uint4*>(img);
-        uint4* dst = reinterpret_cast<uint4*>(tp + ((size_t)chunk * g.Hv + h) * kTPBytes);
-        for (int i = tid; i < (int)(kTPBytes / 16); i += kCT) dst[i] = src[i];
-        __syncthreads();
-    }
+    if (warp == 0) umma::tmem_free(tmem, 512);
 }
 
 // ---- chain ----------------------------------------------------------------------
-// Loads run ahead of the rounds: T and P are double-buffered (chunk c+1's copy is
-// issued when chunk c starts), Q for chunk c+1 is copied as soon as round 1 of
-// chunk c has read it, K as soon as round 3 has, and the V slice and gates of
-// chunk c+1 are fetched into registers while chunk c computes.
+// Per chunk c (b = c & 1), with M = 128 products (a tcgen05 MMA costs the same
+// issue time at M = 64 and M = 128, so operands are stacked):
+//   round A   MMA  [W_c; Q~_c] S0 -> tA[b]: rows 0-63 X = W S0, rows 64-127 Q~ S0
+//             (meanwhile warps 2-3 read O of chunk c-1 out of tA[b^1])
+//             warps 0-1: U = u_c - X -> U image
+//   round B   MMA  K~_c^T U -> tS;  [P_c; P_c] U accumulated onto tA[b], so rows
+//             64-127 become O = Q~ S0 + P U (rows 0-63 are spent)
+//             all: S0 <- gamma_last S0 + tS -> S0 image
+// Copies run ahead: W/Q~ double-buffered two chunks ahead (free once round A of
+// the chunk before has completed), K~ once K~^T U has completed, u once the U
+// rows have been read, and P (twice, for the stacked operand) once P U has.
 template <typename T>
-__global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, const float* __restrict__ y,
-                                                       const int32_t* __restrict__ coff,
-                                                       const unsigned char* __restrict__ kq,
-                                                       const unsigned char* __restrict__ tp) {
+__global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, const int32_t* __restrict__ coff,
+                                                       const ChunkOut ws) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char* ktok = smem;                        // 32 KB  K   [64 tok][2*128]
-    unsigned char* qtok = ktok + kKTokBytes;           // 32 KB  Q   [64 tok][2*128]
-    unsigned char* tpb = qtok + kKTokBytes;            // 2 x 32 KB  T, P [64][2*64]
-    // B operands stored MN-major (rows along K, each thread writes its own row as
-    // 16-byte vectors): S0 [128 key rows][2*32], R, U, diag(c) U [64 tokens][2*32]
-    unsigned char* s0t = tpb + 2 * kTPBytes;           // 16 KB  S0
-    unsigned char* rt = s0t + kNS * 2 * kDK * 2;       //  8 KB  R
-    unsigned char* ut = rt + kNS * 2 * kC * 2;         //  8 KB  U
-    unsigned char* cut = ut + kNS * 2 * kC * 2;        //  8 KB  diag(c) U
-    float* vv = reinterpret_cast<float*>(cut + kNS * 2 * kC * 2);  // [64][32]
-    __shared__ float s_g[kC], s_b[kC], s_G[kC], s_carry;
+    unsigned char* wqb = smem;                        // 2 x 64 KB: [W; Q~] images
+    unsigned char* kt = wqb + 2 * kWQBytes;           // 32 KB: K~ image
+    unsigned char* pp = kt + kImgBytes;               // 32 KB: [P; P] images
+    float* ub = reinterpret_cast<float*>(pp + 2 * kPBytes);  // 8 KB: u rows of this slice
+    // B operands stored MN-major: S0 [128 key rows][2*32], U [64 tokens][2*32]
+    unsigned char* s0t = reinterpret_cast<unsigned char*>(ub + kC * kNS);  // 16 KB
+    unsigned char* ut = s0t + kDK * 2 * kNS * 2;                          //  8 KB
     __shared__ uint32_t s_tmem;
-    __shared__ __align__(8) uint64_t s_k, s_q, s_tp[2], s_mma;
+    __shared__ __align__(8) uint64_t s_wq[2], s_u, s_k, s_p, s_a, s_s, s_o;
     __shared__ int s_abort;
     const Geom& g = a.g;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-    const int hk = h / g.f, col0 = slice * kNS;
+    const int col0 = slice * kNS, nsl = g.dv / kNS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tb = a.cu[n], te = a.cu[n + 1], len = te - tb;
 
@@ -298,7 +537,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             }
     }
     if (len <= 0) return;
-    const int nchunks = coff[n + 1] - coff[n];
+    const int nch = coff[n + 1] - coff[n];
     const int chunk0 = coff[n];
 
     // state rows: thread i holds row i (key dim) of the 32-column slice
@@ -312,213 +551,197 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 #pragma unroll
     for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
 
-    if (warp == 0) umma::tmem_alloc(&s_tmem, 256);
+    if (warp == 0) umma::tmem_alloc(&s_tmem, 128);
     if (tid == 0) {
+        mbar_init(&s_wq[0], 1);
+        mbar_init(&s_wq[1], 1);
+        mbar_init(&s_u, 1);
         mbar_init(&s_k, 1);
-        mbar_init(&s_q, 1);
-        mbar_init(&s_tp[0], 1);
-        mbar_init(&s_tp[1], 1);
-        mbar_init(&s_mma, 1);
+        mbar_init(&s_p, 1);
+        mbar_init(&s_a, 1);
+        mbar_init(&s_s, 1);
+        mbar_init(&s_o, 1);
         fence_mbar_init();
         s_abort = 0;
     }
+    fence_proxy_async_smem();  // S0 image written by the generic proxy
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = s_tmem;
-    const uint32_t tDk = tmem + 0, tDq = tmem + 32, tU = tmem + 64, tO = tmem + 96, tS = tmem + 128;
-    const uint32_t wl = (uint32_t)(32 * warp) << 16;   // this warp's TMEM lane base
-    const int trow = 16 * warp + (lane & 15);         // M = 64 accumulator row held by lanes 0-15
+    const uint32_t tS = tmem, tA0 = tmem + 32;      // tA[b] = tA0 + 32 b
+    const uint32_t wl = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes = accumulator rows 32 warp ..
 
-    // thread 0's bookkeeping of copies and MMAs in flight (for a clean exit on abort)
-    int k_iss = 0, q_iss = 0, tp_iss[2] = {0, 0}, mma_iss = 0;
+    // thread 0's count of copies and MMA commits issued per barrier (for a clean exit on abort)
+    int wq_iss[2] = {0, 0}, u_iss = 0, k_iss = 0, p_iss = 0, a_iss = 0, b_iss = 0;
+    auto rec = [&](int c) { return (size_t)(chunk0 + c) * g.Hv + h; };
+    auto load_wq = [&](int c) {
+        const int b = c & 1;
+        mbar_arrive_expect_tx(&s_wq[b], kWQBytes);
+        bulk_g2s(wqb + b * kWQBytes, ws.wq + rec(c) * kWQBytes, kWQBytes, &s_wq[b]);
+        ++wq_iss[b];
+    };
+    auto load_u = [&](int c) {
+        mbar_arrive_expect_tx(&s_u, kUSlice);
+        bulk_g2s(ub, ws.u + (rec(c) * nsl + slice) * (kC * kNS), kUSlice, &s_u);
+        ++u_iss;
+    };
     auto load_k = [&](int c) {
-        mbar_arrive_expect_tx(&s_k, kKTokBytes);
-        bulk_g2s(ktok, kq + ((size_t)(chunk0 + c) * g.Hk + hk) * kKQBytes, kKTokBytes, &s_k);
+        mbar_arrive_expect_tx(&s_k, kImgBytes);
+        bulk_g2s(kt, ws.kp + rec(c) * kKPBytes, kImgBytes, &s_k);
         ++k_iss;
     };
-    auto load_q = [&](int c) {
-        mbar_arrive_expect_tx(&s_q, kKTokBytes);
-        bulk_g2s(qtok, kq + ((size_t)(chunk0 + c) * g.Hk + hk) * kKQBytes + kKTokBytes, kKTokBytes, &s_q);
-        ++q_iss;
-    };
-    auto load_tp = [&](int c) {
-        const int b = c & 1;
-        mbar_arrive_expect_tx(&s_tp[b], kTPBytes);
-        bulk_g2s(tpb + b * kTPBytes, tp + ((size_t)(chunk0 + c) * g.Hv + h) * kTPBytes, kTPBytes, &s_tp[b]);
-        ++tp_iss[b];
-    };
-    // V slice (16 values per thread) and gates of a chunk, into registers
-    float pv[kC * kNS / kCT], pg = 0.f, pb = 0.f;
-    auto fetch = [&](int c) {
-        const int t0 = tb + c * kC, cnt = min(kC, te - t0);
-#pragma unroll
-        for (int k = 0; k < kC * kNS / kCT; ++k) {
-            const int idx = tid + k * kCT, t = idx / kNS, j = idx - t * kNS;
-            pv[k] = t < cnt ? y[(size_t)(t0 + t) * g.D + 2 * g.Hk * kDK + h * g.dv + col0 + j] : 0.f;
-        }
-        const bool in = tid < cnt;
-        pg = tid < kC && in ? a.gate[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
-        pb = tid < kC && in ? a.beta[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
+    auto load_p = [&](int c) {
+        const unsigned char* src = ws.kp + rec(c) * kKPBytes + kImgBytes;
+        mbar_arrive_expect_tx(&s_p, 2 * kPBytes);
+        bulk_g2s(pp, src, kPBytes, &s_p);
+        bulk_g2s(pp + kPBytes, src, kPBytes, &s_p);
+        ++p_iss;
     };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity)) s_abort = 1;
     };
+    // O rows of chunk cc, by warps 2-3 (rows past the chunk's last token are not stored)
+    auto out_rows = [&](int cc) {
+        wait_all(&s_o, (uint32_t)(cc & 1));
+        umma::fence_after_sync();
+        float ov[kNS];
+        umma::tmem_ld32(tA0 + 32 * (cc & 1) + wl, ov);
+        const int t0 = tb + cc * kC, cnt = min(kC, te - t0), t = 32 * (warp - 2) + lane;
+        if (t < cnt) {
+            float* orow = a.out + ((size_t)(t0 + t) * g.Hv + h) * g.dv + col0;
+#pragma unroll
+            for (int j = 0; j < kNS; j += 4) st_stream(orow + j, make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]));
+        }
+    };
 
     if (tid == 0) {
+        load_wq(0);
+        if (nch > 1) load_wq(1);
+        load_u(0);
         load_k(0);
-        load_q(0);
-        load_tp(0);
+        load_p(0);
     }
-    fetch(0);
-    for (int c = 0; c < nchunks; ++c) {
-        const int t0 = tb + c * kC, cnt = min(kC, te - t0);
-        const unsigned char* tpi = tpb + (c & 1) * kTPBytes;
-        if (tid == 0 && c + 1 < nchunks) load_tp(c + 1);  // its buffer's last reader, chunk c-1, is done
-#pragma unroll
-        for (int k = 0; k < kC * kNS / kCT; ++k) vv[tid + k * kCT] = pv[k];
-        if (tid < kC) {
-            s_g[tid] = pg;
-            s_b[tid] = pb;
-        }
-        __syncthreads();
-        if (c + 1 < nchunks) fetch(c + 1);
-        scan64(s_g, s_G, &s_carry);  // running log-decay; ends with a barrier
-
-        // ---- round 1: K S0 and Q S0 ----
-        wait_all(&s_k, (uint32_t)(c & 1));
-        wait_all(&s_q, (uint32_t)(c & 1));
-        wait_all(&s_tp[c & 1], (uint32_t)((c >> 1) & 1));
-        fence_proxy_async_smem();  // s0t was written by the generic proxy
-        umma::fence_before_sync();
-        __syncthreads();
-        if (s_abort) break;
-        umma::fence_after_sync();
+    for (int c = 0; c < nch; ++c) {
+        const int b = c & 1;
+        const float glc = ws.gl[rec(c)];
+        // ---- round A: [W; Q~] S0 ----
+        wait_all(&s_wq[b], (uint32_t)((c >> 1) & 1));
         if (tid == 0) {
-            umma::mma_split(tDk, ktok, false, s0t, true, kC, kNS, kDK, false);
-            umma::mma_split(tDq, qtok, false, s0t, true, kC, kNS, kDK, false);
-            umma::commit(&s_mma);
-            ++mma_iss;
-        }
-        wait_all(&s_mma, (uint32_t)((3 * c) & 1));
-        umma::fence_after_sync();
-        if (tid == 0 && c + 1 < nchunks) load_q(c + 1);  // round 1 was Q's last reader
-        float dk[kNS], dq[kNS];
-        umma::tmem_ld32(tDk + wl, dk);
-        umma::tmem_ld32(tDq + wl, dq);
-        const float gam_t = expf(s_G[trow]);
-        if (lane < 16) {
-            const float b = s_b[trow];
-            float rr[kNS];
-#pragma unroll
-            for (int j = 0; j < kNS; ++j) rr[j] = __fmul_rn(b, fmaf(-gam_t, dk[j], vv[trow * kNS + j]));
-#pragma unroll
-            for (int j = 0; j < kNS; j += 8) umma::store_split8(rt, trow, j, kNS, rr + j);
-        }
-        fence_proxy_async_smem();
-        umma::fence_before_sync();
-        __syncthreads();
-        if (s_abort) break;
-        umma::fence_after_sync();
-
-        // ---- round 2: U = T R ----
-        if (tid == 0) {
-            umma::mma_split(tU, tpi, false, rt, true, kC, kNS, kC, false);
-            umma::commit(&s_mma);
-            ++mma_iss;
-        }
-        wait_all(&s_mma, (uint32_t)((3 * c + 1) & 1));
-        umma::fence_after_sync();
-        float uu[kNS];
-        umma::tmem_ld32(tU + wl, uu);
-        if (lane < 16) {
-            const float cdec = expf(s_G[kC - 1] - s_G[trow]);
-            float cu[kNS];
-#pragma unroll
-            for (int j = 0; j < kNS; ++j) cu[j] = __fmul_rn(cdec, uu[j]);
-#pragma unroll
-            for (int j = 0; j < kNS; j += 8) {
-                umma::store_split8(ut, trow, j, kNS, uu + j);
-                umma::store_split8(cut, trow, j, kNS, cu + j);
+            umma::mma_split(tA0 + 32 * b, wqb + b * kWQBytes, false, s0t, true, 2 * kC, kNS, kDK, false);
+            umma::commit(&s_a);
+            ++a_iss;
+            if (c > 0) {  // P U of chunk c-1 has completed: the P buffer is free
+                if (!mbar_wait_bounded(&s_o, (uint32_t)((c - 1) & 1))) s_abort = 1;
+                load_p(c);
             }
         }
-        fence_proxy_async_smem();
-        umma::fence_before_sync();
-        __syncthreads();
-        if (s_abort) break;
-        umma::fence_after_sync();
-
-        // ---- round 3: O = diag(gamma) Q S0 + P U;  S += K^T diag(c) U ----
-        if (tid == 0) {
-            umma::mma_split(tO, tpi + kTBytes, false, ut, true, kC, kNS, kC, false);
-            umma::mma_split(tS, ktok, true, cut, true, kDK, kNS, kC, false);
-            umma::commit(&s_mma);
-            ++mma_iss;
-        }
-        wait_all(&s_mma, (uint32_t)((3 * c + 2) & 1));
-        umma::fence_after_sync();
-        if (tid == 0 && c + 1 < nchunks) load_k(c + 1);  // round 3 was K's last reader
-        float oo[kNS], ss[kNS];
-        umma::tmem_ld32(tO + wl, oo);
-        umma::tmem_ld32(tS + wl, ss);
-        if (lane < 16 && trow < cnt) {
-            float* orow = a.out + ((size_t)(t0 + trow) * g.Hv + h) * g.dv + col0;
+        if (warp >= 2) {
+            if (c > 0) out_rows(c - 1);
+        } else {  // U = u - X, rows 0-63
+            wait_all(&s_a, (uint32_t)(c & 1));
+            wait_all(&s_u, (uint32_t)(c & 1));
+            umma::fence_after_sync();
+            float xv[kNS];
+            umma::tmem_ld32(tA0 + 32 * b + wl, xv);
+            const float* ur = ub + tid * kNS;
+            float uu[kNS];
 #pragma unroll
             for (int j = 0; j < kNS; j += 4) {
-                float4 o;
-                o.x = fmaf(gam_t, dq[j], oo[j]); o.y = fmaf(gam_t, dq[j + 1], oo[j + 1]);
-                o.z = fmaf(gam_t, dq[j + 2], oo[j + 2]); o.w = fmaf(gam_t, dq[j + 3], oo[j + 3]);
-                st_stream(orow + j, o);
+                const float4 u4 = *reinterpret_cast<const float4*>(ur + j);
+                uu[j] = __fsub_rn(u4.x, xv[j]);
+                uu[j + 1] = __fsub_rn(u4.y, xv[j + 1]);
+                uu[j + 2] = __fsub_rn(u4.z, xv[j + 2]);
+                uu[j + 3] = __fsub_rn(u4.w, xv[j + 3]);
             }
-        }
-        const float gl = expf(s_G[kC - 1]);
 #pragma unroll
-        for (int j = 0; j < kNS; ++j) S[j] = fmaf(gl, S[j], ss[j]);
+            for (int j = 0; j < kNS; j += 8) umma::store_split8(ut, tid, j, kNS, uu + j);
+        }
+        fence_proxy_async_smem();
+        umma::fence_before_sync();
+        __syncthreads();
+        if (s_abort) break;
+        umma::fence_after_sync();
+
+        // ---- round B: K~^T U and [P; P] U ----
+        if (tid == 0) {
+            if (c + 1 < nch) load_u(c + 1);  // the u rows of chunk c have been read (the barrier above)
+            if (!mbar_wait_bounded(&s_k, (uint32_t)(c & 1))) s_abort = 1;
+            umma::mma_split(tS, kt, true, ut, true, kDK, kNS, kC, false);
+            umma::commit(&s_s);
+            if (!mbar_wait_bounded(&s_p, (uint32_t)(c & 1))) s_abort = 1;
+            umma::mma_split(tA0 + 32 * b, pp, false, ut, true, 2 * kC, kNS, kC, true);
+            umma::commit(&s_o);
+            ++b_iss;
+        }
+        wait_all(&s_s, (uint32_t)(c & 1));
+        umma::fence_after_sync();
+        float ss[kNS];
+        umma::tmem_ld32(tS + wl, ss);
+#pragma unroll
+        for (int j = 0; j < kNS; ++j) S[j] = fmaf(glc, S[j], ss[j]);
 #pragma unroll
         for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
+        if (tid == 0) {
+            if (c + 2 < nch) load_wq(c + 2);  // round A of chunk c has completed: its W/Q~ buffer is free
+            if (c + 1 < nch) load_k(c + 1);   // and K~^T U: the K~ buffer is free
+        }
+        fence_proxy_async_smem();
         umma::fence_before_sync();
-        __syncthreads();  // this chunk's operand reads are complete
+        __syncthreads();
         if (s_abort) break;
         umma::fence_after_sync();
     }
+    if (!s_abort && warp >= 2) out_rows(nch - 1);
     if (s_abort && tid == 0) {
         flag_device_error(&g_chunk_error, 7);
         // let copies and MMAs still in flight land before TMEM and shared memory are released:
         // wait for the last issued phase of each barrier (a completed phase returns at once)
-        if (k_iss) mbar_wait_bounded(&s_k, (uint32_t)((k_iss - 1) & 1));
-        if (q_iss) mbar_wait_bounded(&s_q, (uint32_t)((q_iss - 1) & 1));
         for (int b = 0; b < 2; ++b)
-            if (tp_iss[b]) mbar_wait_bounded(&s_tp[b], (uint32_t)((tp_iss[b] - 1) & 1));
-        if (mma_iss) mbar_wait_bounded(&s_mma, (uint32_t)((mma_iss - 1) & 1));
+            if (wq_iss[b]) mbar_wait_bounded(&s_wq[b], (uint32_t)((wq_iss[b] - 1) & 1));
+        if (u_iss) mbar_wait_bounded(&s_u, (uint32_t)((u_iss - 1) & 1));
+        if (k_iss) mbar_wait_bounded(&s_k, (uint32_t)((k_iss - 1) & 1));
+        if (p_iss) mbar_wait_bounded(&s_p, (uint32_t)((p_iss - 1) & 1));
+        if (a_iss) mbar_wait_bounded(&s_a, (uint32_t)((a_iss - 1) & 1));
+        if (b_iss) {
+            mbar_wait_bounded(&s_s, (uint32_t)((b_iss - 1) & 1));
+            mbar_wait_bounded(&s_o, (uint32_t)((b_iss - 1) & 1));
+        }
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_free(tmem, 256);
+    if (warp == 0) umma::tmem_free(tmem, 128);
     if (s_abort) return;
 #pragma unroll
     for (int j = 0; j < kNS; j += 4) *reinterpret_cast<float4*>(Sg + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
 }
 
-constexpr size_t kChainSmem = 2 * kKTokBytes + 2 * kTPBytes + kNS * 2 * kDK * 2 + 3 * (kNS * 2 * kC * 2) + kC * kNS * 4;
-constexpr size_t kPrepSmem = (4 * kC * (kC + 1) * 4 + kTPBytes) > kKQBytes ? (4 * kC * (kC + 1) * 4 + kTPBytes) : kKQBytes;
+constexpr size_t kChainSmem = 2 * kWQBytes + kImgBytes + 2 * kPBytes + kUSlice + kDK * 2 * kNS * 2 + kC * 2 * kNS * 2;
+static_assert(kChainSmem + 1024 <= 227 * 1024, "chain shared memory");
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct ChunkWs {
-    size_t y, coff, kq, tp, total;
-    ChunkWs(const Geom& g, int N, long long T, int nchunk) {
+    size_t coff, gl, wq, kp, u, total;
+    ChunkWs(const Geom& g, int N, int nchunk) {
+        const size_t recs = (size_t)nchunk * g.Hv;
         size_t o = 0;
-        y = o;    o = align256(o + (size_t)T * g.D * 4);
         coff = o; o = align256(o + (size_t)(N + 1) * 4);
-        kq = o;   o = align256(o + (size_t)nchunk * g.Hk * kKQBytes);
-        tp = o;   o = align256(o + (size_t)nchunk * g.Hv * kTPBytes);
+        gl = o;   o = align256(o + recs * 4);
+        wq = o;   o = align256(o + recs * kWQBytes);
+        kp = o;   o = align256(o + recs * kKPBytes);
+        u = o;    o = align256(o + recs * kC * g.dv * 4);
         total = o;
     }
 };
 
 }  // namespace
 
-bool prefill_chunked_supported(const Geom& g) { return g.dk == kDK && g.dv % kNS == 0; }
+bool prefill_chunked_supported(const Geom& g) {
+    if (g.dk != kDK || g.dv % kNS != 0 || g.dv > kMaxDV || g.K > kKC || g.f > kMaxF) return false;
+    const size_t prep = g.io_bf16 ? PrepSmem<__nv_bfloat16>::total(g.f) : PrepSmem<float>::total(g.f);
+    return prep + 1024 <= 227 * 1024;
+}
 
 int prefill_chunk_count(const int32_t* cu_host, int N) {
     int acc = 0;
@@ -526,53 +749,44 @@ int prefill_chunk_count(const int32_t* cu_host, int N) {
     return acc;
 }
 
-size_t prefill_chunked_workspace(const Geom& g, int N, long long T, int nchunk) {
-    return ChunkWs(g, N, T, nchunk).total;
-}
-
 // The chunk-count-free upper bound used by gdn_prefill_workspace_size:
 // every sequence adds at most one partial chunk.
 size_t prefill_chunked_workspace_bound(const Geom& g, int N, long long T) {
     const long long nchunk = (T + kC - 1) / kC + N;
-    return ChunkWs(g, N, T, (int)std::min<long long>(nchunk, 1ll << 30)).total;
+    return ChunkWs(g, N, (int)std::min<long long>(nchunk, 1ll << 30)).total;
 }
+
+namespace {
+template <typename T>
+cudaError_t launch_chunked_t(const PrefillArgs& a, int nchunk, const int32_t* coff, const ChunkOut& out,
+                             cudaStream_t stream) {
+    const Geom& g = a.g;
+    const size_t prep_smem = PrepSmem<T>::total(g.f);
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
+    if (e != cudaSuccess) return e;
+    chunk_prep_kernel<T><<<dim3(nchunk, g.Hk), kPT, prep_smem, stream>>>(a, coff, out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(chain_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
+    if (e != cudaSuccess) return e;
+    chain_kernel<T><<<dim3(g.dv / kNS, g.Hv, a.N), kCT, kChainSmem, stream>>>(a, coff, out);
+    return cudaGetLastError();
+}
+}  // namespace
 
 cudaError_t launch_prefill_chunked(const PrefillArgs& a, cudaStream_t stream) {
     const Geom& g = a.g;
     const int nchunk = prefill_chunk_count(a.cu_host, a.N);
-    const ChunkWs ws(g, a.N, a.T, nchunk);
+    const ChunkWs ws(g, a.N, nchunk);
     unsigned char* base = static_cast<unsigned char*>(a.ws);
-    float* y = reinterpret_cast<float*>(base + ws.y);
     int32_t* coff = reinterpret_cast<int32_t*>(base + ws.coff);
-    unsigned char* kq = base + ws.kq;
-    unsigned char* tp = base + ws.tp;
-    cudaError_t e = launch_prefill_prep(a, y, stream);
-    if (e != cudaSuccess) return e;
+    const ChunkOut out{base + ws.wq, base + ws.kp, reinterpret_cast<float*>(base + ws.u),
+                       reinterpret_cast<float*>(base + ws.gl)};
     plan_kernel<<<1, 32, 0, stream>>>(a.cu, a.N, coff);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nchunk == 0) return e;
-    if (a.g.io_bf16) {
-        e = cudaFuncSetAttribute(chunk_prep_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPrepSmem);
-        if (e != cudaSuccess) return e;
-        chunk_prep_kernel<__nv_bfloat16><<<dim3(nchunk, g.Hk), kCT, kPrepSmem, stream>>>(a, y, coff, kq, tp);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chain_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kChainSmem);
-        if (e != cudaSuccess) return e;
-        chain_kernel<__nv_bfloat16><<<dim3(g.dv / kNS, g.Hv, a.N), kCT, kChainSmem, stream>>>(a, y, coff, kq, tp);
-    } else {
-        e = cudaFuncSetAttribute(chunk_prep_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
-        if (e != cudaSuccess) return e;
-        chunk_prep_kernel<float><<<dim3(nchunk, g.Hk), kCT, kPrepSmem, stream>>>(a, y, coff, kq, tp);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chain_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
-        if (e != cudaSuccess) return e;
-        chain_kernel<float><<<dim3(g.dv / kNS, g.Hv, a.N), kCT, kChainSmem, stream>>>(a, y, coff, kq, tp);
-    }
-    return cudaGetLastError();
+    return a.g.io_bf16 ? launch_chunked_t<__nv_bfloat16>(a, nchunk, coff, out, stream)
+                       : launch_chunked_t<float>(a, nchunk, coff, out, stream);
 }
 
 cudaError_t chunk_error_read(int32_t* value, bool clear) {
