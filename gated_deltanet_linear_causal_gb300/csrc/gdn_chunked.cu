@@ -217,33 +217,77 @@ __device__ __forceinline__ void conv8(const T* raw, const float* wv, int t, int 
     for (int e = 0; e < 8; ++e) y[e] = silu_fast(acc[e]);
 }
 
-// T = (I + A)^-1 for strictly lower A (row stride kAld): column u (one thread per
-// column) by forward substitution, T[i][u] = -sum_{s<i} A[i][s] T[s][u] for
-// i > u, T[u][u] = 1, four rows at a time (each T[s][u] read once per block, A
-// rows as broadcast float4 reads), into Tb (row stride kLd).
-__device__ __forceinline__ void inverse_column(const float* A, float* Tb, int u) {
-    for (int ib = 0; ib < kC; ib += 4) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-        for (int s = 0; s < ib; s += 4) {
-            const float t0 = Tb[(s + 0) * kLd + u], t1 = Tb[(s + 1) * kLd + u];
-            const float t2 = Tb[(s + 2) * kLd + u], t3 = Tb[(s + 3) * kLd + u];
+// T = (I + A)^-1 for strictly lower A (row stride kAld) into Tb (row stride kLd),
+// by the 256 threads of one group (named barrier `bar`), blocked:
+//   the four 16x16 diagonal blocks by forward substitution, one thread per
+//   column (T[i][u] = -sum_{u<=s<i} A[i][s] T[s][u], T[u][u] = 1);
+//   then for block size B = 16 (two pairs) and B = 32 (one pair) the block
+//   below the diagonal, T21 = -T22 (A21 T11), via scratch X = A21 T11 (the
+//   sums run over whole blocks: the stored zeros of the triangular factors
+//   drop out).
+__device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float* X, int gt, int bar) {
+    constexpr int kG = kPT / 2;
+    if (gt < kC) {
+        const int o = 16 * (gt >> 4), u = gt & 15;
+        float tc[16];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float4 a4 = *reinterpret_cast<const float4*>(A + (ib + r) * kAld + s);
-                acc[r] = fmaf(a4.x, t0, fmaf(a4.y, t1, fmaf(a4.z, t2, fmaf(a4.w, t3, acc[r]))));
-            }
+        for (int i = 0; i < 16; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int s = 0; s < i; ++s) acc = fmaf(A[(o + i) * kAld + o + s], tc[s], acc);
+            tc[i] = i < u ? 0.f : i == u ? 1.f : -acc;
+            Tb[(o + i) * kLd + o + u] = tc[i];
         }
-        float tv[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = ib + r;
-            float sum = acc[r];
+        for (int i = 0; i < 16; ++i)  // the rest of the block row right of the diagonal block
+            for (int jb = o + 16; jb < kC; jb += 16) Tb[(o + i) * kLd + jb + u] = 0.f;
+    }
+    named_sync(bar, kG);
+    // B = 16: the two pairs, element (r, c) of pair p by thread (p's share): gt -> r, c; p = 0, 1
+    {
+        const int r = gt >> 4, c = gt & 15;
+        float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int q = 0; q < r; ++q) sum = fmaf(A[i * kAld + ib + q], tv[q], sum);
-            tv[r] = i < u ? 0.f : i == u ? 1.f : -sum;
-            Tb[i * kLd + u] = tv[r];
+        for (int m = 0; m < 16; ++m) {
+            x0 = fmaf(A[(16 + r) * kAld + m], Tb[m * kLd + c], x0);
+            x1 = fmaf(A[(48 + r) * kAld + 32 + m], Tb[(32 + m) * kLd + 32 + c], x1);
         }
+        X[gt] = x0;
+        X[256 + gt] = x1;
+        named_sync(bar, kG);
+        float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            y0 = fmaf(Tb[(16 + r) * kLd + 16 + m], X[m * 16 + c], y0);
+            y1 = fmaf(Tb[(48 + r) * kLd + 48 + m], X[256 + m * 16 + c], y1);
+        }
+        Tb[(16 + r) * kLd + c] = -y0;
+        Tb[(48 + r) * kLd + 32 + c] = -y1;
+        named_sync(bar, kG);
+    }
+    // B = 32: rows r, r+8, r+16, r+24 and column c of the lower-left block by each thread
+    {
+        const int r = gt >> 5, c = gt & 31;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const float tm = Tb[m * kLd + c];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) x[q] = fmaf(A[(32 + r + 8 * q) * kAld + m], tm, x[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) X[(r + 8 * q) * 32 + c] = x[q];
+        named_sync(bar, kG);
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const float xm = X[m * 32 + c];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[q] = fmaf(Tb[(32 + r + 8 * q) * kLd + 32 + m], xm, y[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Tb[(32 + r + 8 * q) * kLd + c] = -y[q];
+        named_sync(bar, kG);
     }
 }
 
@@ -401,8 +445,7 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                 umma::store_split8(pimg, t, s0, kC, pv);
             }
             named_sync(kBarT, kGrp);
-            if (warp < 2) inverse_column(Ab, Tb, tid);
-            named_sync(kBarT, kGrp);
+            inverse_blocked(Ab, Tb, reinterpret_cast<float*>(timg), tid, kBarT);
             // T diag(beta gamma) and T diag(beta) as A operands
             for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
                 const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
