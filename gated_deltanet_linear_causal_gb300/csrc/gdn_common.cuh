@@ -1,9 +1,10 @@
 // gdn_common.cuh -- device helpers shared by the Gated DeltaNet kernels.
 //
 // The per-token arithmetic of the gated delta rule (MNN discussion "MNN Model
-// Support: Qwen3.5", section 1.2, Step 5) lives here once, in
-// `StateSlice::step`, so that decode, verify and the resident prefill run the
-// same instructions in the same order: a verify snapshot after t tokens is then
+// Support: Qwen3.5", section 1.2, Step 5) for the slice kernels of
+// gdn_step.cu lives here, in `StateSlice::step`, with explicit roundings that
+// match the streaming kernel's `Tile::step`: decode and verify run the same
+// instructions in the same order, so a verify snapshot after t tokens is
 // bitwise equal to t decode calls.
 #pragma once
 

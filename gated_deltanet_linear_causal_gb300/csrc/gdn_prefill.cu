@@ -1,19 +1,20 @@
-// gdn_prefill.cu -- prefill over cu_seqlens-packed sequences, resident form.
+// gdn_prefill.cu -- prefill over cu_seqlens-packed sequences, resident form
+// (GDN_PREFILL_RESIDENT).
 //
-// Two launches:
-//   prep      steps 1-4 of the MNN "Qwen3.5" page, section 1.2, for every packed
-//             token: causal conv + SiLU from the raw qkv [D, T] (channel-major, as
-//             the page lays out qkv [B, D, L]) with each sequence's carried conv
-//             state (section 1.4), then per-head L2 norms and the 1/sqrt(dk)
-//             scale.  Writes token-major fp32 rows y [T, D] to the workspace.
-//   resident  step 5, the gated delta rule: one CTA per (sequence, value head,
-//             32-column slice) keeps its slice of S in registers across the whole
-//             sequence (StateSlice::step, the same arithmetic as decode), with the
-//             next 16 (8 for dk=256) tokens' q/k/v prefetched into registers while the current
-//             16 run from shared memory.  It also writes each sequence's new conv
-//             state: the prep launch has finished reading the old one by then.
-// The resident form is serial in the sequence length: each token waits on the
-// previous one's reductions over dk.
+// Three launches:
+//   prep   steps 1-4 of the MNN "Qwen3.5" page, section 1.2, for every packed
+//          token: causal conv + SiLU from the raw qkv [D, T] (channel-major, as
+//          the page lays out qkv [B, D, L]) with each sequence's carried conv
+//          state (section 1.4), then per-head L2 norms and the 1/sqrt(dk)
+//          scale.  Writes token-major fp32 rows y [T, D] to the workspace.
+//   gram   the lagged dot products q_t.k_{t-d} and k_t.k_{t-d} (d < 8) that the
+//          block recurrence needs, per token and key head.
+//   block  step 5, the gated delta rule: one CTA per (sequence, value head,
+//          column group) keeps its columns of S in registers across the whole
+//          sequence and advances 8 tokens per reduction round (the block form
+//          below).  It also writes each sequence's new conv state: the prep
+//          launch has finished reading the old one by then.
+// The resident form stays serial in the sequence length, 8 tokens at a time.
 #include <algorithm>
 
 #include "gdn_common.cuh"
