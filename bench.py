@@ -258,11 +258,15 @@ def run_decode(args, dev, dist, rank, world, st, steps):
 
 
 def _time_calls(fn, reps, flush):
+    """Device time of one call of fn per repetition, L2 flushed before each.  The flush
+    and a short device-side spin are queued ahead of the start event, so the host's
+    argument marshalling and launch of fn overlap them and stay out of the timed span."""
     import torch
     times = []
     for _ in range(reps):
-        flush()
         torch.cuda.synchronize()
+        flush()
+        torch.cuda._sleep(400_000)  # ~0.2 ms of device time at 2 GHz
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
