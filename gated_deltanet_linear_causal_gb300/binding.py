@@ -39,7 +39,8 @@ class gdn_config_t(ctypes.Structure):
     _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
                 ("conv_kernel", ctypes.c_int32), ("use_qk_l2norm", ctypes.c_int32),
-                ("l2norm_eps", ctypes.c_float), ("io_dtype", ctypes.c_int32)]
+                ("l2norm_eps", ctypes.c_float), ("io_dtype", ctypes.c_int32),
+                ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p)]
 
     @property
     def D(self):
@@ -51,10 +52,24 @@ class gdn_config_t(ctypes.Structure):
 
 
 def make_config(num_k_heads, num_v_heads, head_k_dim, head_v_dim, conv_kernel=4, use_qk_l2norm=True,
-                l2norm_eps=1e-6, io_dtype="bf16") -> gdn_config_t:
+                l2norm_eps=1e-6, io_dtype="bf16", A_log=None, dt_bias=None) -> gdn_config_t:
+    """A_log, dt_bias: optional CUDA fp32 tensors of num_v_heads; when given, the gate
+    and beta tensors of every call are the raw projections a and b (see include/gdn.h).
+    The config keeps references to them for as long as it lives."""
     io = {"bf16": GDN_BF16, "f32": GDN_F32}[io_dtype] if isinstance(io_dtype, str) else int(io_dtype)
-    return gdn_config_t(num_k_heads, num_v_heads, head_k_dim, head_v_dim, conv_kernel, int(bool(use_qk_l2norm)),
-                        l2norm_eps, io)
+    if (A_log is None) != (dt_bias is None):
+        raise ValueError("A_log and dt_bias go together")
+    ptrs = (None, None)
+    if A_log is not None:
+        for name, t in (("A_log", A_log), ("dt_bias", dt_bias)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+                    and t.numel() == num_v_heads):
+                raise ValueError(f"{name}: expected a contiguous CUDA float32 tensor of {num_v_heads} elements")
+        ptrs = (A_log.data_ptr(), dt_bias.data_ptr())
+    cfg = gdn_config_t(num_k_heads, num_v_heads, head_k_dim, head_v_dim, conv_kernel, int(bool(use_qk_l2norm)),
+                       l2norm_eps, io, *ptrs)
+    cfg._keep = (A_log, dt_bias)
+    return cfg
 
 
 _lib = None

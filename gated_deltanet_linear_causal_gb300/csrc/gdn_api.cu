@@ -47,6 +47,8 @@ gdn_status_t check_config(const gdn_config_t* c, gdn::Geom* g) {
     g->eps = c->l2norm_eps;
     g->q_scale = (float)(1.0 / std::sqrt((double)c->head_k_dim));
     g->io_bf16 = c->io_dtype == GDN_BF16;
+    if ((c->A_log == nullptr) != (c->dt_bias == nullptr)) return GDN_ERR_NULL;
+    if (c->A_log && (!aligned(c->A_log, 4) || !aligned(c->dt_bias, 4))) return GDN_ERR_ALIGN;
     return GDN_OK;
 }
 
@@ -135,7 +137,7 @@ gdn_status_t gdn_forward_decode(const gdn_config_t* cfg, int32_t batch, const vo
     a.conv_out = conv_state;
     a.S_out = ssm_state;
     a.out = out;
-    return cuda_status(gdn::launch_step(a, true, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(gdn::launch_step(a, gdn::GateParams{cfg->A_log, cfg->dt_bias}, true, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gdn_status_t gdn_forward_verify(const gdn_config_t* cfg, int32_t batch, int32_t L, const void* qkv,
@@ -168,7 +170,7 @@ gdn_status_t gdn_forward_verify(const gdn_config_t* cfg, int32_t batch, int32_t 
     a.conv_out = conv_snap;
     a.S_out = ssm_snap;
     a.out = out;
-    return cuda_status(gdn::launch_step(a, false, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(gdn::launch_step(a, gdn::GateParams{cfg->A_log, cfg->dt_bias}, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gdn_status_t gdn_verify_commit(const gdn_config_t* cfg, int32_t batch, int32_t L, const int32_t* accepted,
@@ -254,8 +256,9 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, cons
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return cuda_status(variant == GDN_PREFILL_CHUNKED ? gdn::launch_prefill_chunked(a, s)
-                                                      : gdn::launch_prefill_resident(a, s));
+    const gdn::GateParams gp{cfg->A_log, cfg->dt_bias};
+    return cuda_status(variant == GDN_PREFILL_CHUNKED ? gdn::launch_prefill_chunked(a, gp, s)
+                                                      : gdn::launch_prefill_resident(a, gp, s));
 }
 
 }  // extern "C"

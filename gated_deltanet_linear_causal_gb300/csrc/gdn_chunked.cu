@@ -293,7 +293,7 @@ __device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float
 
 template <typename T>
 __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a, const int32_t* __restrict__ coff,
-                                                            const ChunkOut ws) {
+                                                            const ChunkOut ws, const GateParams gp) {
     using L = PrepSmem<T>;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* kimg = smem + L::kimg;
@@ -333,8 +333,8 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     for (int idx = tid; idx < f * kC; idx += kPT) {
         const int j = idx / kC, t = idx - j * kC;
         const bool in = t < cnt;
-        sG[idx] = in ? a.gate[(size_t)(t0 + t) * g.Hv + hk * f + j] : 0.f;
-        sBet[idx] = in ? a.beta[(size_t)(t0 + t) * g.Hv + hk * f + j] : 0.f;
+        sG[idx] = in ? gate_of(gp.A_log, gp.dt_bias, a.gate[(size_t)(t0 + t) * g.Hv + hk * f + j], hk * f + j) : 0.f;
+        sBet[idx] = in ? beta_of(gp.A_log, a.beta[(size_t)(t0 + t) * g.Hv + hk * f + j]) : 0.f;
     }
 
     // ---- steps 1-4 for Q, then K: conv + SiLU, L2 norm (1/sqrt(dk) for Q) ----
@@ -801,13 +801,13 @@ size_t prefill_chunked_workspace_bound(const Geom& g, int N, long long T) {
 
 namespace {
 template <typename T>
-cudaError_t launch_chunked_t(const PrefillArgs& a, int nchunk, const int32_t* coff, const ChunkOut& out,
-                             cudaStream_t stream) {
+cudaError_t launch_chunked_t(const PrefillArgs& a, const GateParams& gp, int nchunk, const int32_t* coff,
+                             const ChunkOut& out, cudaStream_t stream) {
     const Geom& g = a.g;
     const size_t prep_smem = PrepSmem<T>::total(g.f);
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
-    chunk_prep_kernel<T><<<dim3(nchunk, g.Hk), kPT, prep_smem, stream>>>(a, coff, out);
+    chunk_prep_kernel<T><<<dim3(nchunk, g.Hk), kPT, prep_smem, stream>>>(a, coff, out, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chain_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
@@ -817,7 +817,7 @@ cudaError_t launch_chunked_t(const PrefillArgs& a, int nchunk, const int32_t* co
 }
 }  // namespace
 
-cudaError_t launch_prefill_chunked(const PrefillArgs& a, cudaStream_t stream) {
+cudaError_t launch_prefill_chunked(const PrefillArgs& a, const GateParams& gp, cudaStream_t stream) {
     const Geom& g = a.g;
     const int nchunk = prefill_chunk_count(a.cu_host, a.N);
     const ChunkWs ws(g, a.N, nchunk);
@@ -828,8 +828,8 @@ cudaError_t launch_prefill_chunked(const PrefillArgs& a, cudaStream_t stream) {
     plan_kernel<<<1, 32, 0, stream>>>(a.cu, a.N, coff);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nchunk == 0) return e;
-    return a.g.io_bf16 ? launch_chunked_t<__nv_bfloat16>(a, nchunk, coff, out, stream)
-                       : launch_chunked_t<float>(a, nchunk, coff, out, stream);
+    return a.g.io_bf16 ? launch_chunked_t<__nv_bfloat16>(a, gp, nchunk, coff, out, stream)
+                       : launch_chunked_t<float>(a, gp, nchunk, coff, out, stream);
 }
 
 cudaError_t chunk_error_read(int32_t* value, bool clear) {

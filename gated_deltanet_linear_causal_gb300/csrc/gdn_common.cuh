@@ -40,6 +40,21 @@ __device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpr
 
 __device__ __forceinline__ float silu(float y) { return y / (1.f + expf(-y)); }
 
+// Gate parameterisation of section 1.2: with per-value-head A_log and dt_bias
+// set, the gate input is the raw projection a and the log-decay is
+// -exp(A_log[h]) * softplus(a + dt_bias[h]), softplus(x) = log(1 + e^x) (x
+// itself above 20, where the two agree in fp32); the beta input is the raw b
+// and the rate is sigmoid(b).  Without them the inputs are used as they are.
+__device__ __forceinline__ float gate_of(const float* A_log, const float* dt_bias, float raw, int h) {
+    if (!A_log) return raw;
+    const float x = raw + dt_bias[h];
+    const float sp = x > 20.f ? x : log1pf(expf(x));
+    return -expf(A_log[h]) * sp;
+}
+__device__ __forceinline__ float beta_of(const float* A_log, float raw) {
+    return A_log ? 1.f / (1.f + expf(-raw)) : raw;
+}
+
 // ---- thread-block cluster barrier (sm_90+) ----------------------------------
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");

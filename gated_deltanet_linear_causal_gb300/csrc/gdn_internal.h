@@ -17,6 +17,15 @@ struct Geom {
     int io_bf16;    // 1: bf16 storage, 0: fp32 storage
 };
 
+// Gate parameterisation (section 1.2): per-value-head A_log and dt_bias, or both
+// NULL when the gate/beta inputs are the log-decay and rate themselves.  Passed
+// to the kernels as a parameter of its own: the argument structs stay as they are
+// (growing StepArgs by these 16 bytes cost the decode kernel about 5 %).
+struct GateParams {
+    const float* A_log;    // [Hv]
+    const float* dt_bias;  // [Hv]
+};
+
 // Decode (in place, L = 1) and verify (snapshots, L tokens) share one kernel.
 struct StepArgs {
     Geom g;
@@ -34,9 +43,9 @@ struct StepArgs {
 // Decode / verify.  launch_step picks the persistent TMA-fed kernel
 // (gdn_stream.cu) when stream_step_supported() accepts the shape, else the
 // cluster-per-key-head slice kernel (gdn_step.cu).
-cudaError_t launch_step(const StepArgs& a, bool in_place, cudaStream_t stream);
+cudaError_t launch_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream);
 bool stream_step_supported(const StepArgs& a, int* nstage, size_t* smem_bytes);
-cudaError_t launch_stream_step(const StepArgs& a, bool in_place, cudaStream_t stream);
+cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream);
 bool slice_step_supported(const Geom& g);
 cudaError_t stream_error_read(int32_t* value, bool clear);
 
@@ -74,14 +83,14 @@ struct PrefillArgs {
     size_t ws_bytes;
 };
 size_t prefill_resident_workspace(const Geom& g, int N, long long T);
-cudaError_t launch_prefill_resident(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_resident(const PrefillArgs& a, const GateParams& gp, cudaStream_t stream);
 // Steps 1-4 for every packed token into token-major normalised fp32 rows y [T, D].
 cudaError_t launch_prefill_prep(const PrefillArgs& a, float* y, cudaStream_t stream);
 
 // Chunked (tensor-core) prefill, gdn_chunked.cu.
 bool prefill_chunked_supported(const Geom& g);
 size_t prefill_chunked_workspace_bound(const Geom& g, int N, long long T);
-cudaError_t launch_prefill_chunked(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_chunked(const PrefillArgs& a, const GateParams& gp, cudaStream_t stream);
 cudaError_t chunk_error_read(int32_t* value, bool clear);
 
 }  // namespace gdn

@@ -238,7 +238,7 @@ struct BlockCfg {
 };
 
 template <typename T, int DK>
-__global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const float* __restrict__ y,
+__global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const GateParams gp, const float* __restrict__ y,
                                                     const float* __restrict__ gram) {
     using R = BlockCfg<DK>;
     constexpr int RPL = R::RPL, KR = R::KR, LPC = R::LPC, CPW = R::CPW, kBC = R::BC;
@@ -298,8 +298,8 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const f
             pre[j] = v;
         }
         const bool ok = tid < kBM && t0 + tid < te;
-        pg = ok ? a.gate[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
-        pb = ok ? a.beta[(size_t)(t0 + tid) * g.Hv + h] : 0.f;
+        pg = ok ? gate_of(gp.A_log, gp.dt_bias, a.gate[(size_t)(t0 + tid) * g.Hv + h], h) : 0.f;
+        pb = ok ? beta_of(gp.A_log, a.beta[(size_t)(t0 + tid) * g.Hv + h]) : 0.f;
         pgr = (tid < kBM * 16 && t0 + (tid >> 4) < te) ? __ldg(gram + ((size_t)(t0 + (tid >> 4)) * g.Hk + hk) * 16 + (tid & 15))
                                                       : 0.f;
     };
@@ -436,7 +436,7 @@ cudaError_t launch_prep_t(const PrefillArgs& a, float* y, cudaStream_t stream) {
 }
 
 template <typename T, int DK>
-cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
+cudaError_t launch_resident_t(const PrefillArgs& a, const GateParams& gp, cudaStream_t stream) {
     const Geom& g = a.g;
     float* y = static_cast<float*>(a.ws);
     float* gram = y + (size_t)a.T * g.D;
@@ -448,7 +448,7 @@ cudaError_t launch_resident_t(const PrefillArgs& a, cudaStream_t stream) {
     gram_kernel<DK><<<dim3((a.T + kGramTok - 1) / kGramTok, g.Hk), 256, gram_smem, stream>>>(a, y, gram);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    block_kernel<T, DK><<<dim3(g.dv / BlockCfg<DK>::BC, g.Hv, a.N), kBT, 0, stream>>>(a, y, gram);
+    block_kernel<T, DK><<<dim3(g.dv / BlockCfg<DK>::BC, g.Hv, a.N), kBT, 0, stream>>>(a, gp, y, gram);
     return cudaGetLastError();
 }
 
@@ -462,20 +462,20 @@ size_t prefill_resident_workspace(const Geom& g, int /*N*/, long long T) {
     return (size_t)T * g.D * sizeof(float) + (size_t)T * g.Hk * 16 * sizeof(float);
 }
 
-cudaError_t launch_prefill_resident(const PrefillArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_resident(const PrefillArgs& a, const GateParams& gp, cudaStream_t s) {
     if (a.g.io_bf16) {
         switch (a.g.dk) {
-            case 32: return launch_resident_t<__nv_bfloat16, 32>(a, s);
-            case 64: return launch_resident_t<__nv_bfloat16, 64>(a, s);
-            case 128: return launch_resident_t<__nv_bfloat16, 128>(a, s);
-            case 256: return launch_resident_t<__nv_bfloat16, 256>(a, s);
+            case 32: return launch_resident_t<__nv_bfloat16, 32>(a, gp, s);
+            case 64: return launch_resident_t<__nv_bfloat16, 64>(a, gp, s);
+            case 128: return launch_resident_t<__nv_bfloat16, 128>(a, gp, s);
+            case 256: return launch_resident_t<__nv_bfloat16, 256>(a, gp, s);
         }
     } else {
         switch (a.g.dk) {
-            case 32: return launch_resident_t<float, 32>(a, s);
-            case 64: return launch_resident_t<float, 64>(a, s);
-            case 128: return launch_resident_t<float, 128>(a, s);
-            case 256: return launch_resident_t<float, 256>(a, s);
+            case 32: return launch_resident_t<float, 32>(a, gp, s);
+            case 64: return launch_resident_t<float, 64>(a, gp, s);
+            case 128: return launch_resident_t<float, 128>(a, gp, s);
+            case 256: return launch_resident_t<float, 256>(a, gp, s);
         }
     }
     return cudaErrorInvalidValue;

@@ -27,7 +27,7 @@ namespace gdn {
 namespace {
 
 template <typename T, int DK, bool IN_PLACE>
-__global__ void __launch_bounds__(kStepThreads) step_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kStepThreads) step_kernel(const StepArgs a, const GateParams gp) {
     extern __shared__ float4 smem_f4[];
     float* sm = reinterpret_cast<float*>(smem_f4);
     const Geom& g = a.g;
@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const StepArgs a) {
     const int cq = StateSlice<DK>::cq(), rg = StateSlice<DK>::rg();
     for (int t = 0; t < L; ++t) {
         const size_t gi = ((size_t)b * L + t) * g.Hv + h;
-        const float alpha = expf(a.gate[gi]);
-        const float bt = a.beta[gi];
+        const float alpha = expf(gate_of(gp.A_log, gp.dt_bias, a.gate[gi], h));
+        const float bt = beta_of(gp.A_log, a.beta[gi]);
         const float4 v4 = *reinterpret_cast<const float4*>(v_s + t * kSliceCols + 4 * cq);
         const float4 o = S.step(qk_s + t * 2 * DK + DK, qk_s + t * 2 * DK, v4, alpha, bt, coef[3 * t + 2],
                                 red + (t & 1) * 256);
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const StepArgs a) {
 }
 
 template <typename T, int DK, bool IN_PLACE>
-cudaError_t launch_step_t(const StepArgs& a, cudaStream_t stream) {
+cudaError_t launch_step_t(const StepArgs& a, const GateParams& gp, cudaStream_t stream) {
     const Geom& g = a.g;
     const int NS = g.dv / kSliceCols;
     const size_t floats = (size_t)a.L * (2 * DK + kSliceCols) + 4 * 3 * kMaxVerify + 3 * kMaxVerify + 2 * 4 * 64;
@@ -180,24 +180,24 @@ cudaError_t launch_step_t(const StepArgs& a, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, a, gp);
 }
 
 template <bool IN_PLACE>
-cudaError_t dispatch_step(const StepArgs& a, cudaStream_t s) {
+cudaError_t dispatch_step(const StepArgs& a, const GateParams& gp, cudaStream_t s) {
     if (a.g.io_bf16) {
         switch (a.g.dk) {
-            case 32: return launch_step_t<__nv_bfloat16, 32, IN_PLACE>(a, s);
-            case 64: return launch_step_t<__nv_bfloat16, 64, IN_PLACE>(a, s);
-            case 128: return launch_step_t<__nv_bfloat16, 128, IN_PLACE>(a, s);
-            case 256: return launch_step_t<__nv_bfloat16, 256, IN_PLACE>(a, s);
+            case 32: return launch_step_t<__nv_bfloat16, 32, IN_PLACE>(a, gp, s);
+            case 64: return launch_step_t<__nv_bfloat16, 64, IN_PLACE>(a, gp, s);
+            case 128: return launch_step_t<__nv_bfloat16, 128, IN_PLACE>(a, gp, s);
+            case 256: return launch_step_t<__nv_bfloat16, 256, IN_PLACE>(a, gp, s);
         }
     } else {
         switch (a.g.dk) {
-            case 32: return launch_step_t<float, 32, IN_PLACE>(a, s);
-            case 64: return launch_step_t<float, 64, IN_PLACE>(a, s);
-            case 128: return launch_step_t<float, 128, IN_PLACE>(a, s);
-            case 256: return launch_step_t<float, 256, IN_PLACE>(a, s);
+            case 32: return launch_step_t<float, 32, IN_PLACE>(a, gp, s);
+            case 64: return launch_step_t<float, 64, IN_PLACE>(a, gp, s);
+            case 128: return launch_step_t<float, 128, IN_PLACE>(a, gp, s);
+            case 256: return launch_step_t<float, 256, IN_PLACE>(a, gp, s);
         }
     }
     return cudaErrorInvalidValue;
@@ -251,11 +251,11 @@ __global__ void zero_kernel(unsigned char* p, size_t head, size_t n16, size_t ta
 
 bool slice_step_supported(const Geom& g) { return (g.dv / kSliceCols) * g.f <= 16; }
 
-cudaError_t launch_step(const StepArgs& a, bool in_place, cudaStream_t stream) {
+cudaError_t launch_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream) {
     int ns = 0;
     size_t smem = 0;
-    if (stream_step_supported(a, &ns, &smem)) return launch_stream_step(a, in_place, stream);
-    return in_place ? dispatch_step<true>(a, stream) : dispatch_step<false>(a, stream);
+    if (stream_step_supported(a, &ns, &smem)) return launch_stream_step(a, gp, in_place, stream);
+    return in_place ? dispatch_step<true>(a, gp, stream) : dispatch_step<false>(a, gp, stream);
 }
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {

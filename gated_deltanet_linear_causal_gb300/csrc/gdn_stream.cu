@@ -137,8 +137,10 @@ __device__ __forceinline__ TileRef tile_ref(const Geom& g, int item, int r) {
     return t;
 }
 
-template <typename T, int DK, bool IN_PLACE>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, const int nstage) {
+// RAW: the gate/beta inputs are raw projections (the config carries A_log and
+// dt_bias); a separate instantiation keeps the plain path's prologue unchanged.
+template <typename T, int DK, bool IN_PLACE, bool RAW>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, const int nstage, const GateParams gp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ int s_abort;    // any role gave up: the others stop waiting
     __shared__ int s_cabort;   // compute group's own flag (uniform decisions)
@@ -244,8 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             for (int idx = pt; idx < L * g.f; idx += kProlog) {
                 const int t = idx / g.f, hl = idx - t * g.f;
                 const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
-                ab[2 * idx + 0] = expf(a.gate[gi]);
-                ab[2 * idx + 1] = a.beta[gi];
+                if (RAW) {
+                    ab[2 * idx + 0] = expf(gate_of(gp.A_log, gp.dt_bias, a.gate[gi], hk * g.f + hl));
+                    ab[2 * idx + 1] = beta_of(gp.A_log, a.beta[gi]);
+                } else {
+                    ab[2 * idx + 0] = expf(a.gate[gi]);
+                    ab[2 * idx + 1] = a.beta[gi];
+                }
             }
             // Groups of CG consecutive channels per thread, all loads of a group issued
             // before any is used.  The Q, K and V ranges are multiples of CG long.
@@ -382,13 +389,13 @@ int sm_count() {
 }
 
 template <typename T, int DK, bool IN_PLACE>
-cudaError_t launch_t(const StepArgs& a, int nstage, size_t smem, cudaStream_t stream) {
-    auto kern = stream_kernel<T, DK, IN_PLACE>;
+cudaError_t launch_t(const StepArgs& a, const GateParams& gp, int nstage, size_t smem, cudaStream_t stream) {
+    auto kern = gp.A_log ? stream_kernel<T, DK, IN_PLACE, true> : stream_kernel<T, DK, IN_PLACE, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nitems = a.B * a.g.Hk;
     const int grid = std::min(nitems, sm_count());
-    kern<<<grid, kThreads, smem, stream>>>(a, nstage);
+    kern<<<grid, kThreads, smem, stream>>>(a, nstage, gp);
     return cudaGetLastError();
 }
 
@@ -409,19 +416,19 @@ bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out)
     return false;
 }
 
-cudaError_t launch_stream_step(const StepArgs& a, bool in_place, cudaStream_t s) {
+cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t s) {
     int ns = 0;
     size_t smem = 0;
     if (!stream_step_supported(a, &ns, &smem)) return cudaErrorInvalidValue;
     const bool bf = a.g.io_bf16;
     if (a.g.dk == 128) {
-        if (bf) return in_place ? launch_t<__nv_bfloat16, 128, true>(a, ns, smem, s)
-                                : launch_t<__nv_bfloat16, 128, false>(a, ns, smem, s);
-        return in_place ? launch_t<float, 128, true>(a, ns, smem, s) : launch_t<float, 128, false>(a, ns, smem, s);
+        if (bf) return in_place ? launch_t<__nv_bfloat16, 128, true>(a, gp, ns, smem, s)
+                                : launch_t<__nv_bfloat16, 128, false>(a, gp, ns, smem, s);
+        return in_place ? launch_t<float, 128, true>(a, gp, ns, smem, s) : launch_t<float, 128, false>(a, gp, ns, smem, s);
     }
-    if (bf) return in_place ? launch_t<__nv_bfloat16, 64, true>(a, ns, smem, s)
-                            : launch_t<__nv_bfloat16, 64, false>(a, ns, smem, s);
-    return in_place ? launch_t<float, 64, true>(a, ns, smem, s) : launch_t<float, 64, false>(a, ns, smem, s);
+    if (bf) return in_place ? launch_t<__nv_bfloat16, 64, true>(a, gp, ns, smem, s)
+                            : launch_t<__nv_bfloat16, 64, false>(a, gp, ns, smem, s);
+    return in_place ? launch_t<float, 64, true>(a, gp, ns, smem, s) : launch_t<float, 64, false>(a, gp, ns, smem, s);
 }
 
 cudaError_t stream_error_read(int32_t* value, bool clear) {

@@ -250,6 +250,16 @@ def verify_block(seed=5, batch=32, L=4, shape=PRODUCTION):
     )
 
 
+def raw_gates(seed, lead, num_v_heads):
+    """Stand-ins for the raw gate inputs of section 1.2's parameterisation (no trained
+    weights exist here): projections a, b ~ N(0, 1) float32 shaped lead + (H_v,), and
+    per-head A_log, dt_bias ~ N(0, 0.5) float32 [H_v]."""
+    d = Draw(seed)
+    shape = tuple(lead) + (num_v_heads,)
+    return dict(a=d.f32("a", shape), b=d.f32("bproj", shape),
+                A_log=d.f32("A_log", (num_v_heads,), 0.0, 0.5), dt_bias=d.f32("dt_bias", (num_v_heads,), 0.0, 0.5))
+
+
 def as_f64(arr: np.ndarray, io: str) -> np.ndarray:
     """Exact float64 values of stored inputs (bf16 bits or float32)."""
     if arr.dtype == np.uint16:

@@ -81,6 +81,16 @@ typedef struct {
     int32_t use_qk_l2norm; /* 0 or 1 */
     float l2norm_eps;      /* eps in x / sqrt(sum x^2 + eps); 1e-6 is the usual value */
     int32_t io_dtype;      /* gdn_dtype_t */
+    /* Gate parameterisation (section 1.2, "gate is carefully parameterized").
+     * Both NULL: the `gate` and `beta` arguments of every call are the log-decay
+     * g_t (<= 0) and the rate beta_t themselves.  Both set: they are the raw
+     * projections a_t and b_t, and the kernels form, per value head h,
+     *   gate = -exp(A_log[h]) * softplus(a + dt_bias[h]),  beta = sigmoid(b),
+     * with softplus(x) = log(1 + e^x) (x itself above 20).  Device arrays of
+     * num_v_heads fp32, 4-byte aligned, caller-owned, read by every call that
+     * uses the config.  Only one of the two set: GDN_ERR_NULL. */
+    const float *A_log;
+    const float *dt_bias;
 } gdn_config_t;
 
 /* Prefill variants. */

@@ -66,8 +66,9 @@ def open_library(path: str):
                                        i64, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.gdn_oracle_forward_work_doubles.argtypes = [i64] * 5
     lib.gdn_oracle_forward_work_doubles.restype = i64
+    lib.gdn_oracle_gate_beta.argtypes = [i64, i64, P, P, P, P, P, P]
     for f in (lib.gdn_oracle_conv1d_silu, lib.gdn_oracle_split_norm_scale,
-              lib.gdn_oracle_delta_rule, lib.gdn_oracle_forward):
+              lib.gdn_oracle_delta_rule, lib.gdn_oracle_forward, lib.gdn_oracle_gate_beta):
         f.restype = None
     return lib
 
@@ -131,6 +132,20 @@ class Cfg:
 # ---------------------------------------------------------------------------
 # Single steps (each pinned on its own by the tests).
 # ---------------------------------------------------------------------------
+
+def gate_beta(a, b, A_log, dt_bias):
+    """Gate parameterisation of section 1.2: from the raw projections a, b [.., H]
+    and the per-head A_log, dt_bias [H], gate = -exp(A_log) * softplus(a + dt_bias)
+    and beta = sigmoid(b).  Returns (gate, beta), float64, shaped like a."""
+    a = _in(a)
+    b = _in(b, a.shape)
+    H = a.shape[-1]
+    A_log = _in(A_log, (H,))
+    dt_bias = _in(dt_bias, (H,))
+    gate, beta = np.empty_like(a), np.empty_like(a)
+    _load().gdn_oracle_gate_beta(a.size // H, H, _p(a), _p(b), _p(A_log), _p(dt_bias), _p(gate), _p(beta))
+    return gate, beta
+
 
 def conv1d_silu(x, w, state_in, snapshots=False):
     """Step 1 over one sequence. x [D, L], w [D, K], state_in [D, K-1].

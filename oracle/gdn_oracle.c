@@ -206,6 +206,27 @@ void gdn_oracle_forward(int64_t Hk, int64_t Hv, int64_t dk, int64_t dv, int64_t 
     gdn_oracle_delta_rule(Hv, dk, dv, L, q, kk, v, g, beta, S_in, o, S_out, S_snap, rw);
 }
 
+/* ---- Gate parameterisation (section 1.2, after Step 5) ------------------- */
+/*
+ * From the raw projections a, b [n][H] and the per-head parameters A_log,
+ * dt_bias [H]:
+ *   gate[t][h] = -exp(A_log[h]) * softplus(a[t][h] + dt_bias[h]),
+ *   beta[t][h] = sigmoid(b[t][h]) = 1 / (1 + exp(-b[t][h])),
+ * with softplus(x) = log(1 + exp(x)), written as max(x, 0) + log1p(exp(-|x|))
+ * (the same number, without overflow for large x).
+ */
+void gdn_oracle_gate_beta(int64_t n, int64_t H, const double *a, const double *b,
+                          const double *A_log, const double *dt_bias,
+                          double *gate, double *beta) {
+    for (int64_t t = 0; t < n; ++t)
+        for (int64_t h = 0; h < H; ++h) {
+            const double x = a[t * H + h] + dt_bias[h];
+            const double sp = (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+            gate[t * H + h] = -exp(A_log[h]) * sp;
+            beta[t * H + h] = 1.0 / (1.0 + exp(-b[t * H + h]));
+        }
+}
+
 int64_t gdn_oracle_forward_work_doubles(int64_t Hk, int64_t Hv, int64_t dk,
                                         int64_t dv, int64_t L)
 {

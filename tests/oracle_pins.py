@@ -350,4 +350,34 @@ def pin_forward_snapshots_are_prefix_runs():
         _close(full["conv_snap"][t], p["conv"], rtol=0, atol=0, what=f"conv snap {t}")
 
 
+# ---- gate parameterisation (section 1.2) -------------------------------------
+
+def pin_gate_beta_closed_forms():
+    # softplus(0) = ln 2, sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, exp(ln 2) = 2
+    a = np.array([[0.0, -0.5, 2.0]])
+    b = np.array([[0.0, np.log(3.0), -np.log(3.0)]])
+    A_log = np.array([0.0, np.log(2.0), 0.0])
+    dt_bias = np.array([0.0, 0.5, -2.0])
+    g, beta = oracle.gate_beta(a, b, A_log, dt_bias)
+    _close(g, [[-np.log(2.0), -2.0 * np.log(2.0), -np.log(2.0)]], what="gate closed forms")
+    _close(beta, [[0.5, 0.75, 0.25]], what="beta closed forms")
+
+
+def pin_gate_beta_library():
+    r = _rng(41)
+    a, b = r.normal(0, 3, (6, 5)), r.normal(0, 3, (6, 5))
+    A_log, dt_bias = r.normal(0, 1, 5), r.normal(0, 1, 5)
+    g, beta = oracle.gate_beta(a, b, A_log, dt_bias)
+    _close(g, -np.exp(A_log) * np.logaddexp(0.0, a + dt_bias), what="gate vs numpy.logaddexp")
+    _close(beta, scipy.special.expit(b), what="beta vs scipy expit")
+    assert np.all(g <= 0.0) and np.all(np.exp(g) <= 1.0), "decay above 1"
+
+
+def pin_gate_large_argument():
+    # softplus(x) -> x for large x, -> e^x for very negative x
+    g, _ = oracle.gate_beta(np.array([[60.0, -40.0]]), np.zeros((1, 2)), np.array([0.5, 0.0]), np.array([0.0, 0.0]))
+    _close(g[0, 0], -np.exp(0.5) * 60.0, what="softplus large x")
+    _close(g[0, 1], -np.exp(-40.0), rtol=1e-12, atol=0.0, what="softplus very negative x")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -64,6 +64,15 @@ def test_config_validation(lib):
     assert _decode(lib, _cfg(head_k_dim=32, head_v_dim=512, num_v_heads=64)) == 8
     assert lib.gdn_forward_decode(None, 1, *[FAKE] * 7, None) == 1
     assert binding.gdn_status_string(8).startswith("shape or variant")
+    # gate parameterisation: A_log and dt_bias together, 4-byte aligned
+    half = _cfg()
+    half.A_log = FAKE
+    assert _decode(lib, half) == 1                             # dt_bias missing
+    odd = _cfg()
+    odd.A_log, odd.dt_bias = FAKE, FAKE + 2
+    assert _decode(lib, odd) == 3
+    with pytest.raises(ValueError):
+        binding.make_config(16, 32, 128, 128, A_log=object())
 
 
 def test_pointer_validation(lib):

@@ -28,6 +28,12 @@ MUTATIONS = {
     "eps_dropped": ("const double nq = sqrt(sq + eps), nk = sqrt(sk + eps);",
                     "const double nq = sqrt(sq), nk = sqrt(sk);"),
     "v_from_key_head": ("vt[j] = y[(v0 + h * dv + j) * L + t];", "vt[j] = y[(v0 + hk * dv + j) * L + t];"),
+    "gate_sign": ("gate[t * H + h] = -exp(A_log[h]) * sp;", "gate[t * H + h] = exp(A_log[h]) * sp;"),
+    "gate_no_dt_bias": ("const double x = a[t * H + h] + dt_bias[h];", "const double x = a[t * H + h];"),
+    "softplus_as_relu": ("const double sp = (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));",
+                         "const double sp = (x > 0.0 ? x : 0.0);"),
+    "beta_sign": ("beta[t * H + h] = 1.0 / (1.0 + exp(-b[t * H + h]));",
+                  "beta[t * H + h] = 1.0 / (1.0 + exp(b[t * H + h]));"),
 }
 
 
