@@ -309,6 +309,50 @@ def run_decode_raw_gates(dev, st, steps, n_steps=128):
     return e0.elapsed_time(e1) / n_steps
 
 
+def run_decode_gated(dev, st, steps, n_steps=128):
+    """Decode B=64 with the gated RMSNorm (section 2) fused into the output epilogue:
+    bf16 z in, bf16 y out instead of the fp32 output.  Returns ms per step."""
+    import torch
+    from gated_deltanet_linear_causal_gb300 import binding as gb, synth
+    n_in = len(steps)
+    d = synth.Draw(8)
+    cfg = gb.make_config(16, 32, 128, 128, 4, True, 1e-6, "bf16")
+    qkv = torch.stack([_to_dev(s["qkv"], dev) for s in steps])
+    gate = torch.stack([_to_dev(s["gate"], dev) for s in steps])
+    beta = torch.stack([_to_dev(s["beta"], dev) for s in steps])
+    z = _to_dev(d.bf16("z", (n_in, B_DECODE, 32, 128)), dev)
+    w_n = _to_dev(d.f32("norm_w", (128,), 1.0, 0.3), dev)
+    w = _to_dev(st["conv_weight"], dev)
+    S = [_to_dev(st["ssm_state"], dev) for _ in range(2)]
+    conv = [_to_dev(st["conv_state"], dev) for _ in range(2)]
+    y = torch.empty(B_DECODE, 32, 128, dtype=torch.bfloat16, device=dev)
+
+    out = torch.empty(B_DECODE, 32, 128, device=dev)
+
+    def step(i):
+        j, r = i % n_in, i % 2
+        gb.gdn_forward_decode_gated(cfg, B_DECODE, qkv[j], w, gate[j], beta[j], conv[r], S[r], z[j], w_n, 1e-6, y)
+
+    def step_unfused(i):  # the same through gdn_forward_decode, then the standalone norm
+        j, r = i % n_in, i % 2
+        gb.gdn_forward_decode(cfg, B_DECODE, qkv[j], w, gate[j], beta[j], conv[r], S[r], out)
+        gb.gdn_gated_rmsnorm(cfg, B_DECODE * 32, out, z[j], w_n, 1e-6, y)
+
+    res = []
+    for fn in (step, step_unfused):
+        for i in range(8):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n_steps):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        res.append(e0.elapsed_time(e1) / n_steps)
+    return res
+
+
 def run_prefill(dev, x, variant, reps=5):
     import numpy as np
     import torch
@@ -456,6 +500,12 @@ def main():
                                        "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                        "algorithmic_bytes": nb,
                                        "note": "gate = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) in the kernel"}
+        ms, ms_unfused = run_decode_gated(dev, st, steps)
+        nb = decode_bytes(shape, B_DECODE) - B_DECODE * 32 * 128 * 4 + 2 * B_DECODE * 32 * 128 * 2 + 128 * 4
+        sec["decode_B64_gated_norm"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),
+                                        "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                        "algorithmic_bytes": nb, "ms_decode_then_norm_kernel": round(ms_unfused, 5),
+                                        "note": "gated RMSNorm fused: bf16 z in, bf16 y out"}
         mv, mc = run_verify(dev, x_ver)
         nb = verify_bytes(shape, 32, 4)
         sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4),

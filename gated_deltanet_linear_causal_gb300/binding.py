@@ -26,7 +26,7 @@ GDN_PREFILL_RESIDENT, GDN_PREFILL_CHUNKED = 0, 1
 
 EXPORTED = ("gdn_conv_state_init", "gdn_forward_decode", "gdn_prefill_workspace_size", "gdn_forward_prefill",
             "gdn_forward_verify", "gdn_verify_commit", "gdn_status_string", "gdn_last_cuda_error",
-            "gdn_device_error")
+            "gdn_device_error", "gdn_gated_rmsnorm", "gdn_forward_decode_gated")
 
 
 class GdnError(RuntimeError):
@@ -102,8 +102,10 @@ def load(path: str | None = None):
         lib.gdn_last_cuda_error.restype = i32
         lib.gdn_device_error.argtypes = [ctypes.POINTER(i32), i32]
         lib.gdn_device_error.restype = i32
+        lib.gdn_gated_rmsnorm.argtypes = [cfgp, i64, vp, vp, vp, ctypes.c_float, vp, vp]
+        lib.gdn_forward_decode_gated.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
         for name in ("gdn_conv_state_init", "gdn_forward_decode", "gdn_forward_prefill", "gdn_forward_verify",
-                     "gdn_verify_commit"):
+                     "gdn_verify_commit", "gdn_gated_rmsnorm", "gdn_forward_decode_gated"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -163,6 +165,36 @@ def gdn_forward_decode(cfg, batch, qkv, conv_weight, gate, beta, conv_state, ssm
             _dev("ssm_state", ssm_state, torch.float32, batch * H * cfg.head_k_dim * cfg.head_v_dim),
             _dev("out", out, torch.float32, batch * H * cfg.head_v_dim)]
     _check("gdn_forward_decode", load().gdn_forward_decode(ctypes.byref(cfg), batch, *args, _stream(stream)))
+
+
+def gdn_gated_rmsnorm(cfg, rows, o, z, weight, eps, y, stream=None):
+    """Gated RMSNorm (section 2) over rows of head_v_dim: y = weight * o / rms(o) * silu(z).
+    o: CUDA fp32 [rows, dv]; z, y: io dtype [rows, dv]; weight: fp32 [dv]."""
+    if rows == 0:
+        return
+    dv, io = cfg.head_v_dim, cfg.torch_dtype
+    args = [_dev("o", o, torch.float32, rows * dv), _dev("z", z, io, rows * dv), _dev("weight", weight, torch.float32, dv)]
+    _check("gdn_gated_rmsnorm", load().gdn_gated_rmsnorm(ctypes.byref(cfg), rows, *args, float(eps),
+                                                         _dev("y", y, io, rows * dv), _stream(stream)))
+
+
+def gdn_forward_decode_gated(cfg, batch, qkv, conv_weight, gate, beta, conv_state, ssm_state, z, norm_weight, norm_eps,
+                             y, stream=None):
+    """gdn_forward_decode with the gated RMSNorm fused into the output: y (io dtype
+    [batch, Hv, dv]) instead of the fp32 output."""
+    if batch == 0:
+        return
+    D, K, H, dv = cfg.D, cfg.conv_kernel, cfg.num_v_heads, cfg.head_v_dim
+    io = cfg.torch_dtype
+    args = [_dev("qkv", qkv, io, batch * D), _dev("conv_weight", conv_weight, io, D * K),
+            _dev("gate", gate, torch.float32, batch * H), _dev("beta", beta, torch.float32, batch * H),
+            _dev("conv_state", conv_state, io, batch * D * (K - 1)),
+            _dev("ssm_state", ssm_state, torch.float32, batch * H * cfg.head_k_dim * dv),
+            _dev("z", z, io, batch * H * dv), _dev("norm_weight", norm_weight, torch.float32, dv)]
+    _check("gdn_forward_decode_gated", load().gdn_forward_decode_gated(ctypes.byref(cfg), batch, *args,
+                                                                       float(norm_eps),
+                                                                       _dev("y", y, io, batch * H * dv),
+                                                                       _stream(stream)))
 
 
 def gdn_prefill_workspace_size(cfg, num_seqs, total_tokens, variant=GDN_PREFILL_RESIDENT):

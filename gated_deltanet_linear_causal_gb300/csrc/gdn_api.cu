@@ -140,6 +140,60 @@ gdn_status_t gdn_forward_decode(const gdn_config_t* cfg, int32_t batch, const vo
     return cuda_status(gdn::launch_step(a, gdn::GateParams{cfg->A_log, cfg->dt_bias}, true, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+gdn_status_t gdn_gated_rmsnorm(const gdn_config_t* cfg, int64_t rows, const float* o, const void* z,
+                               const float* weight, float eps, void* y, gdn_stream_t stream) {
+    gdn::Geom g;
+    gdn_status_t st = check_config(cfg, &g);
+    if (st != GDN_OK) return st;
+    if (rows < 0 || !(eps >= 0.f) || !std::isfinite(eps)) return GDN_ERR_SHAPE;
+    if (rows == 0) return GDN_OK;
+    if (!o || !z || !weight || !y) return GDN_ERR_NULL;
+    if (!aligned(o, 16) || !aligned(z, 16) || !aligned(weight, 16) || !aligned(y, 16)) return GDN_ERR_ALIGN;
+    return cuda_status(gdn::launch_gated_rmsnorm(g, rows, o, z, weight, eps, y, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status_t gdn_forward_decode_gated(const gdn_config_t* cfg, int32_t batch, const void* qkv, const void* conv_weight,
+                                      const float* gate, const float* beta, void* conv_state, float* ssm_state,
+                                      const void* z, const float* norm_weight, float norm_eps, void* y,
+                                      gdn_stream_t stream) {
+    gdn::Geom g;
+    gdn_status_t st = check_config(cfg, &g);
+    if (st != GDN_OK) return st;
+    if (batch < 0 || batch > 65535 || !(norm_eps >= 0.f) || !std::isfinite(norm_eps)) return GDN_ERR_SHAPE;
+    {
+        gdn::StepArgs probe{};
+        probe.g = g;
+        probe.B = batch;
+        probe.L = 1;
+        int ns = 0;
+        size_t sm = 0;
+        if (g.dv != 128 || !gdn::stream_step_supported(probe, &ns, &sm)) return GDN_ERR_UNSUPPORTED;
+    }
+    if (batch == 0) return GDN_OK;
+    if (!qkv || !conv_weight || !gate || !beta || (!conv_state && g.K > 1) || !ssm_state || !z || !norm_weight || !y)
+        return GDN_ERR_NULL;
+    const size_t eb = elem_bytes(cfg);
+    if (!aligned(qkv, 16) || !aligned(ssm_state, 16) || !aligned(z, 16) || !aligned(y, 16) || !aligned(norm_weight, 16) ||
+        !aligned(conv_weight, eb) || !aligned(conv_state, eb) || !aligned(gate, 4) || !aligned(beta, 4))
+        return GDN_ERR_ALIGN;
+    gdn::StepArgs a{};
+    a.g = g;
+    a.B = batch;
+    a.L = 1;
+    a.qkv = qkv;
+    a.w = conv_weight;
+    a.gate = gate;
+    a.beta = beta;
+    a.conv_in = conv_state;
+    a.S_in = ssm_state;
+    a.conv_out = conv_state;
+    a.S_out = ssm_state;
+    a.out = nullptr;
+    const gdn::NormParams np{z, norm_weight, norm_eps, y};
+    return cuda_status(gdn::launch_step(a, gdn::GateParams{cfg->A_log, cfg->dt_bias}, true,
+                                        reinterpret_cast<cudaStream_t>(stream), np));
+}
+
 gdn_status_t gdn_forward_verify(const gdn_config_t* cfg, int32_t batch, int32_t L, const void* qkv,
                                 const void* conv_weight, const float* gate, const float* beta,
                                 const void* conv_state, const float* ssm_state, void* conv_snap, float* ssm_snap,

@@ -43,9 +43,21 @@ struct StepArgs {
 // Decode / verify.  launch_step picks the persistent TMA-fed kernel
 // (gdn_stream.cu) when stream_step_supported() accepts the shape, else the
 // cluster-per-key-head slice kernel (gdn_step.cu).
-cudaError_t launch_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream);
+// Gated RMSNorm (section 2) fused into the decode output epilogue: y instead of out.
+struct NormParams {
+    const void* z;         // [B, Hv, dv] io dtype; NULL: no fused norm
+    const float* weight;   // [dv]
+    float eps;
+    void* y;               // [B, Hv, dv] io dtype
+};
+cudaError_t launch_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream,
+                        const NormParams& np = NormParams{});
 bool stream_step_supported(const StepArgs& a, int* nstage, size_t* smem_bytes);
-cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream);
+cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream,
+                               const NormParams& np = NormParams{});
+// Standalone gated RMSNorm over rows of dv (gdn_norm.cu).
+cudaError_t launch_gated_rmsnorm(const Geom& g, long long rows, const float* o, const void* z, const float* weight,
+                                 float eps, void* y, cudaStream_t stream);
 bool slice_step_supported(const Geom& g);
 cudaError_t stream_error_read(int32_t* value, bool clear);
 

@@ -251,10 +251,12 @@ __global__ void zero_kernel(unsigned char* p, size_t head, size_t n16, size_t ta
 
 bool slice_step_supported(const Geom& g) { return (g.dv / kSliceCols) * g.f <= 16; }
 
-cudaError_t launch_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream) {
+cudaError_t launch_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t stream,
+                        const NormParams& np) {
     int ns = 0;
     size_t smem = 0;
-    if (stream_step_supported(a, &ns, &smem)) return launch_stream_step(a, gp, in_place, stream);
+    if (stream_step_supported(a, &ns, &smem)) return launch_stream_step(a, gp, in_place, stream, np);
+    if (np.z) return cudaErrorInvalidValue;  // the fused norm lives in the streaming kernel only
     return in_place ? dispatch_step<true>(a, gp, stream) : dispatch_step<false>(a, gp, stream);
 }
 

@@ -107,7 +107,7 @@ struct Tile {
 
 // Shared-memory carve-up (dynamic part).
 struct Layout {
-    size_t stage, qk, v, coef, ab, nred, red, bars, total;
+    size_t stage, qk, v, coef, ab, nred, red, zs, bars, total;
     __host__ __device__ Layout(int DK, int nstage, int L, int f, int dv) {
         size_t o = 0;
         stage = o; o += (size_t)nstage * DK * kTileCols * 4;
@@ -117,6 +117,7 @@ struct Layout {
         ab = o;    o += (size_t)2 * L * f * 2 * 4;            // exp(gate), beta per token and value head
         nred = o;  o += (size_t)kPrologWarps * 3 * kMaxVerify * 4;
         red = o;   o += (size_t)2 * kComputeWarps * 256 * 4;
+        zs = o;    o += L == 1 ? (size_t)(nstage + 1) * f * dv * 4 : 0;  // decode: gated-norm z, nstage+1 items
         bars = o;  o += (size_t)(2 * nstage + 4) * 8;         // full[ns], empty[ns], qfull[2], qempty[2]
         total = o;
     }
@@ -137,10 +138,43 @@ __device__ __forceinline__ TileRef tile_ref(const Geom& g, int item, int r) {
     return t;
 }
 
+// Gated RMSNorm (section 2) of one value head's output row, which every compute
+// warp holds after Tile::step (dv = 128: lane l has columns 4l..4l+3 in o):
+// y = weight * o / sqrt(mean(o^2) + eps) * silu(z), written in the io type.
+// Every warp forms the row's sum of squares; warp w writes the columns of lanes
+// l with l % 8 == w, spreading the gate arithmetic over the eight warps.  `at` is
+// the row's first element index, zrow the row's z, copied into shared memory by
+// the producer with the item's first state tile.
+template <typename T>
+__device__ __forceinline__ void norm_out(const NormParams& np, size_t at, float4 o, int dv, const T* zrow) {
+    const int lane = threadIdx.x & 31, c = 4 * lane;
+    float ss = __fmul_rn(o.x, o.x);
+    ss = fmaf(o.y, o.y, ss);
+    ss = fmaf(o.z, o.z, ss);
+    ss = fmaf(o.w, o.w, ss);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rinv = rsqrtf(fmaf(ss, 1.f / (float)dv, np.eps));
+    if ((lane & (kComputeWarps - 1)) != (int)(threadIdx.x >> 5)) return;
+    const float4 w4 = __ldg(reinterpret_cast<const float4*>(np.weight + c));
+    T* yr = static_cast<T*>(np.y) + at + c;
+    const float ov[4] = {o.x, o.y, o.z, o.w}, wv[4] = {w4.x, w4.y, w4.z, w4.w};
+    float zv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zv[e] = to_f32(zrow[c + e]);
+    T yv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) yv[e] = from_f32<T>(__fmul_rn(__fmul_rn(wv[e], __fmul_rn(ov[e], rinv)), silu(zv[e])));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) yr[e] = yv[e];
+}
+
 // RAW: the gate/beta inputs are raw projections (the config carries A_log and
-// dt_bias); a separate instantiation keeps the plain path's prologue unchanged.
-template <typename T, int DK, bool IN_PLACE, bool RAW>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, const int nstage, const GateParams gp) {
+// dt_bias); NORM: the gated RMSNorm epilogue writes y instead of the output.
+// Separate instantiations keep the plain path unchanged.
+template <typename T, int DK, bool IN_PLACE, bool RAW, bool NORM>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, const int nstage, const GateParams gp,
+                                                             const NormParams np) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ int s_abort;    // any role gave up: the others stop waiting
     __shared__ int s_cabort;   // compute group's own flag (uniform decisions)
@@ -162,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
     float* ab_buf = reinterpret_cast<float*>(smem_raw + lay.ab);
     float* nred = reinterpret_cast<float*>(smem_raw + lay.nred);
     float* red = reinterpret_cast<float*>(smem_raw + lay.red);
+    float* zs_buf = reinterpret_cast<float*>(smem_raw + lay.zs);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + lay.bars);
     uint64_t* empty = full + nstage;
     uint64_t* qfull = empty + nstage;
@@ -201,10 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             const TileRef tr = tile_ref(g, (int)blockIdx.x + (j / tpi) * (int)gridDim.x, j % tpi);
             const float* src = a.S_in + ((size_t)(tr.b * g.Hv + tr.h) * DK) * g.dv + tr.col0;
             float* dst = stage + (size_t)s * TILE;
+            // gated norm (dv == 128, one tile per value head): the item's z rides on its first
+            // tile's barrier, into buffer item % (nstage + 1): the ring runs at most nstage
+            // tiles, so fewer than nstage + 1 items, ahead of the oldest tile in use
+            const bool zcopy = NORM && j % tpi == 0;
+            const uint32_t zbytes = (uint32_t)(g.f * g.dv * sizeof(T));
             if (lane == 0) {
                 fence_proxy_async_smem();  // the compute warps' reads of this stage come first
-                mbar_arrive_expect_tx(full + s, TILE * 4);
+                mbar_arrive_expect_tx(full + s, TILE * 4 + (zcopy ? zbytes : 0));
                 if (g.dv == kTileCols) bulk_g2s(dst, src, TILE * 4, full + s);
+                if (zcopy)
+                    bulk_g2s(reinterpret_cast<T*>(zs_buf) + (size_t)((j / tpi) % (nstage + 1)) * g.f * g.dv,
+                             static_cast<const T*>(np.z) + ((size_t)tr.b * g.Hv + tr.hk * g.f) * g.dv, zbytes, full + s);
             }
             if (g.dv != kTileCols) {
                 __syncwarp();
@@ -243,15 +286,20 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
             float* coef = coef_buf + buf * 3 * kMaxVerify;
             float* ab = ab_buf + (size_t)buf * L * g.f * 2;
-            for (int idx = pt; idx < L * g.f; idx += kProlog) {
-                const int t = idx / g.f, hl = idx - t * g.f;
-                const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
-                if (RAW) {
-                    ab[2 * idx + 0] = expf(gate_of(gp.A_log, gp.dt_bias, a.gate[gi], hk * g.f + hl));
-                    ab[2 * idx + 1] = beta_of(gp.A_log, a.beta[gi]);
-                } else {
-                    ab[2 * idx + 0] = expf(a.gate[gi]);
-                    ab[2 * idx + 1] = a.beta[gi];
+            // gate/beta of the item: the first values per thread
+            // are loaded here and stored after the conv loop, so that their trip to
+            // memory overlaps the conv inputs' instead of preceding it
+            constexpr int kPG = 2;
+            float pgv[kPG], pbv[kPG];
+#pragma unroll
+            for (int m = 0; m < kPG; ++m) {
+                const int idx = pt + m * kProlog;
+                pgv[m] = pbv[m] = 0.f;
+                if (idx < L * g.f) {
+                    const int t = idx / g.f, hl = idx - t * g.f;
+                    const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
+                    pgv[m] = a.gate[gi];
+                    pbv[m] = a.beta[gi];
                 }
             }
             // Groups of CG consecutive channels per thread, all loads of a group issued
@@ -285,6 +333,24 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
 #pragma unroll
                     for (int u = 0; u < CG; ++u) win[u].store_state(cout + ((size_t)b * g.D + cc[u]) * (g.K - 1), g.K);
                 }
+            }
+            auto put_ab = [&](int idx, float gv, float bv) {
+                const int hl = idx % g.f;
+                if (RAW) {
+                    ab[2 * idx + 0] = expf(gate_of(gp.A_log, gp.dt_bias, gv, hk * g.f + hl));
+                    ab[2 * idx + 1] = beta_of(gp.A_log, bv);
+                } else {
+                    ab[2 * idx + 0] = expf(gv);
+                    ab[2 * idx + 1] = bv;
+                }
+            };
+#pragma unroll
+            for (int m = 0; m < kPG; ++m)
+                if (pt + m * kProlog < L * g.f) put_ab(pt + m * kProlog, pgv[m], pbv[m]);
+            for (int idx = pt + kPG * kProlog; idx < L * g.f; idx += kProlog) {
+                const int t = idx / g.f, hl = idx - t * g.f;
+                const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
+                put_ab(idx, a.gate[gi], a.beta[gi]);
             }
             named_sync(kBarProlog, kProlog);
             for (int t = 0; t < L; ++t) {
@@ -366,7 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 const float4 o = S.step(qk + t * 2 * DK + DK, qk + t * 2 * DK, v4, alpha, bt, coef[3 * t + 2],
                                         red + (ustep & 1) * kComputeWarps * 256);
                 ++ustep;
-                if (warp == 0) st_stream(a.out + gi * g.dv + tr.col0 + Tile<DK>::col4(), o);
+                if (NORM)
+                    norm_out<T>(np, gi * g.dv, o, g.dv,
+                                reinterpret_cast<const T*>(zs_buf) + (size_t)(i % (nstage + 1)) * g.f * g.dv +
+                                    tr.hl * g.dv);
+                else if (warp == 0) st_stream(a.out + gi * g.dv + tr.col0 + Tile<DK>::col4(), o);
                 if (!IN_PLACE) S.store_global(a.S_out + (gi * DK) * g.dv + tr.col0, g.dv);
             }
             if (IN_PLACE) S.store_global(a.S_out + ((size_t)(tr.b * g.Hv + tr.h) * DK) * g.dv + tr.col0, g.dv);
@@ -389,13 +459,17 @@ int sm_count() {
 }
 
 template <typename T, int DK, bool IN_PLACE>
-cudaError_t launch_t(const StepArgs& a, const GateParams& gp, int nstage, size_t smem, cudaStream_t stream) {
-    auto kern = gp.A_log ? stream_kernel<T, DK, IN_PLACE, true> : stream_kernel<T, DK, IN_PLACE, false>;
+cudaError_t launch_t(const StepArgs& a, const GateParams& gp, const NormParams& np, int nstage, size_t smem,
+                     cudaStream_t stream) {
+    auto kern = gp.A_log ? stream_kernel<T, DK, IN_PLACE, true, false> : stream_kernel<T, DK, IN_PLACE, false, false>;
+    if constexpr (IN_PLACE) {
+        if (np.z) kern = gp.A_log ? stream_kernel<T, DK, true, true, true> : stream_kernel<T, DK, true, false, true>;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nitems = a.B * a.g.Hk;
     const int grid = std::min(nitems, sm_count());
-    kern<<<grid, kThreads, smem, stream>>>(a, nstage, gp);
+    kern<<<grid, kThreads, smem, stream>>>(a, nstage, gp, np);
     return cudaGetLastError();
 }
 
@@ -416,19 +490,21 @@ bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out)
     return false;
 }
 
-cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t s) {
+cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t s,
+                               const NormParams& np) {
+    if (np.z && (!in_place || a.g.dv != kTileCols)) return cudaErrorInvalidValue;
     int ns = 0;
     size_t smem = 0;
     if (!stream_step_supported(a, &ns, &smem)) return cudaErrorInvalidValue;
     const bool bf = a.g.io_bf16;
     if (a.g.dk == 128) {
-        if (bf) return in_place ? launch_t<__nv_bfloat16, 128, true>(a, gp, ns, smem, s)
-                                : launch_t<__nv_bfloat16, 128, false>(a, gp, ns, smem, s);
-        return in_place ? launch_t<float, 128, true>(a, gp, ns, smem, s) : launch_t<float, 128, false>(a, gp, ns, smem, s);
+        if (bf) return in_place ? launch_t<__nv_bfloat16, 128, true>(a, gp, np, ns, smem, s)
+                                : launch_t<__nv_bfloat16, 128, false>(a, gp, np, ns, smem, s);
+        return in_place ? launch_t<float, 128, true>(a, gp, np, ns, smem, s) : launch_t<float, 128, false>(a, gp, np, ns, smem, s);
     }
-    if (bf) return in_place ? launch_t<__nv_bfloat16, 64, true>(a, gp, ns, smem, s)
-                            : launch_t<__nv_bfloat16, 64, false>(a, gp, ns, smem, s);
-    return in_place ? launch_t<float, 64, true>(a, gp, ns, smem, s) : launch_t<float, 64, false>(a, gp, ns, smem, s);
+    if (bf) return in_place ? launch_t<__nv_bfloat16, 64, true>(a, gp, np, ns, smem, s)
+                            : launch_t<__nv_bfloat16, 64, false>(a, gp, np, ns, smem, s);
+    return in_place ? launch_t<float, 64, true>(a, gp, np, ns, smem, s) : launch_t<float, 64, false>(a, gp, np, ns, smem, s);
 }
 
 cudaError_t stream_error_read(int32_t* value, bool clear) {

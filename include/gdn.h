@@ -231,6 +231,41 @@ gdn_status_t gdn_verify_commit(const gdn_config_t *cfg, int32_t batch, int32_t L
                                float *ssm_state, int32_t *status,
                                gdn_stream_t stream);
 
+/*
+ * Gated RMSNorm of the layer output (section 2, "Gated RMSNorm", as the linear
+ * attention layer applies it: attn_out = norm(attn_out, z)).  For every row r
+ * (one token of one value head):
+ *   y[r][j] = weight[j] * o[r][j] / sqrt(mean_i o[r][i]^2 + eps) * silu(z[r][j]),
+ * silu(x) = x / (1 + e^-x); the norm runs over head_v_dim, the last axis of
+ * the output as laid out ([.., Hv, dv]), and weight is shared by the heads.
+ *   rows     number of rows: tokens * num_v_heads (0 is a no-op)
+ *   o        device [rows, dv] fp32 (the output of any forward call), 16-byte aligned
+ *   z        device [rows, dv] io dtype (the gate projection), 16-byte aligned
+ *   weight   device [dv] fp32, 16-byte aligned
+ *   eps      >= 0
+ *   y        device [rows, dv] io dtype (bf16 output for bf16 io), 16-byte aligned;
+ *            may be o itself only for fp32 io
+ */
+gdn_status_t gdn_gated_rmsnorm(const gdn_config_t *cfg, int64_t rows, const float *o,
+                               const void *z, const float *weight, float eps, void *y,
+                               gdn_stream_t stream);
+
+/*
+ * A decode step with the gated RMSNorm fused into the output epilogue: as
+ * gdn_forward_decode, but instead of the fp32 output it writes
+ *   y    device [batch, Hv, dv] io dtype, gdn_gated_rmsnorm of the step's output
+ * from z (device [batch, Hv, dv] io dtype), norm_weight (device [dv] fp32) and
+ * norm_eps.  Built for the persistent decode kernel with head_v_dim = 128 (one
+ * state tile per value head holds the whole row being normalised); other shapes
+ * return GDN_ERR_UNSUPPORTED (call gdn_forward_decode, then gdn_gated_rmsnorm).
+ */
+gdn_status_t gdn_forward_decode_gated(const gdn_config_t *cfg, int32_t batch,
+                                      const void *qkv, const void *conv_weight,
+                                      const float *gate, const float *beta,
+                                      void *conv_state, float *ssm_state,
+                                      const void *z, const float *norm_weight,
+                                      float norm_eps, void *y, gdn_stream_t stream);
+
 /* Static description of a status code. */
 const char *gdn_status_string(gdn_status_t status);
 

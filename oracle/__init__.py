@@ -67,8 +67,10 @@ def open_library(path: str):
     lib.gdn_oracle_forward_work_doubles.argtypes = [i64] * 5
     lib.gdn_oracle_forward_work_doubles.restype = i64
     lib.gdn_oracle_gate_beta.argtypes = [i64, i64, P, P, P, P, P, P]
+    lib.gdn_oracle_gated_rmsnorm.argtypes = [i64, i64, P, P, P, ctypes.c_double, P]
     for f in (lib.gdn_oracle_conv1d_silu, lib.gdn_oracle_split_norm_scale,
-              lib.gdn_oracle_delta_rule, lib.gdn_oracle_forward, lib.gdn_oracle_gate_beta):
+              lib.gdn_oracle_delta_rule, lib.gdn_oracle_forward, lib.gdn_oracle_gate_beta,
+              lib.gdn_oracle_gated_rmsnorm):
         f.restype = None
     return lib
 
@@ -145,6 +147,18 @@ def gate_beta(a, b, A_log, dt_bias):
     gate, beta = np.empty_like(a), np.empty_like(a)
     _load().gdn_oracle_gate_beta(a.size // H, H, _p(a), _p(b), _p(A_log), _p(dt_bias), _p(gate), _p(beta))
     return gate, beta
+
+
+def gated_rmsnorm(o, z, weight, eps):
+    """Gated RMSNorm of section 2 over the last axis: weight * o / sqrt(mean(o^2) + eps)
+    * silu(z).  o, z [.., n]; weight [n].  Returns float64 shaped like o."""
+    o = _in(o)
+    z = _in(z, o.shape)
+    n = o.shape[-1]
+    weight = _in(weight, (n,))
+    y = np.empty_like(o)
+    _load().gdn_oracle_gated_rmsnorm(o.size // n, n, _p(o), _p(z), _p(weight), float(eps), _p(y))
+    return y
 
 
 def conv1d_silu(x, w, state_in, snapshots=False):

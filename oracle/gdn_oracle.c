@@ -227,6 +227,26 @@ void gdn_oracle_gate_beta(int64_t n, int64_t H, const double *a, const double *b
         }
 }
 
+/* ---- Gated RMSNorm of the layer output (section 2) ----------------------- */
+/*
+ * For each of `rows` rows of n values:
+ *   y[r][j] = weight[j] * o[r][j] / sqrt(mean_i o[r][i]^2 + eps) * silu(z[r][j]),
+ * silu(a) = a / (1 + e^-a).  The rows are the (token, value head) pairs of the
+ * layer output; n = head_v_dim.
+ */
+void gdn_oracle_gated_rmsnorm(int64_t rows, int64_t n, const double *o, const double *z,
+                              const double *weight, double eps, double *y) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double sq = 0.0;
+        for (int64_t j = 0; j < n; ++j) sq += o[r * n + j] * o[r * n + j];
+        const double rms = sqrt(sq / (double)n + eps);
+        for (int64_t j = 0; j < n; ++j) {
+            const double zz = z[r * n + j];
+            y[r * n + j] = weight[j] * (o[r * n + j] / rms) * (zz / (1.0 + exp(-zz)));
+        }
+    }
+}
+
 int64_t gdn_oracle_forward_work_doubles(int64_t Hk, int64_t Hv, int64_t dk,
                                         int64_t dv, int64_t L)
 {

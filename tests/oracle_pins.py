@@ -380,4 +380,29 @@ def pin_gate_large_argument():
     _close(g[0, 1], -np.exp(-40.0), rtol=1e-12, atol=0.0, what="softplus very negative x")
 
 
+# ---- gated RMSNorm (section 2) ------------------------------------------------
+
+def pin_gated_rmsnorm_numpy():
+    r = _rng(43)
+    o, z = r.normal(0, 2, (5, 3, 8)), r.normal(0, 2, (5, 3, 8))
+    w = r.normal(1, 0.3, 8)
+    y = oracle.gated_rmsnorm(o, z, w, 1e-6)
+    rms = np.linalg.norm(o, axis=-1, keepdims=True) / np.sqrt(8.0)
+    ref = w * (o / np.sqrt(rms ** 2 + 1e-6)) * _silu(z)
+    _close(y, ref, what="gated RMSNorm vs numpy")
+
+
+def pin_gated_rmsnorm_closed_forms():
+    # a constant row c with unit weight and eps = 0 normalises to sign(c); z = 0 gates to 0;
+    # silu(ln 3) = (3/4) ln 3
+    o = np.array([[-2.5] * 4, [3.0, -3.0, 3.0, -3.0]])
+    z = np.array([[np.log(3.0)] * 4, [0.0, 1.0, 0.0, 1.0]])
+    y = oracle.gated_rmsnorm(o, z, np.ones(4), 0.0)
+    _close(y[0], [-0.75 * np.log(3.0)] * 4, what="constant row")
+    _close(y[1], [0.0, -scipy.special.expit(1.0), 0.0, -scipy.special.expit(1.0)], what="z = 0 and z = 1")
+    # eps: a row of zeros stays finite and zero
+    y0 = oracle.gated_rmsnorm(np.zeros((1, 4)), np.ones((1, 4)), np.ones(4), 1e-6)
+    _close(y0, np.zeros((1, 4)), what="zero row")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

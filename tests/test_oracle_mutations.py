@@ -34,6 +34,10 @@ MUTATIONS = {
                          "const double sp = (x > 0.0 ? x : 0.0);"),
     "beta_sign": ("beta[t * H + h] = 1.0 / (1.0 + exp(-b[t * H + h]));",
                   "beta[t * H + h] = 1.0 / (1.0 + exp(b[t * H + h]));"),
+    "rmsnorm_sum_not_mean": ("const double rms = sqrt(sq / (double)n + eps);", "const double rms = sqrt(sq + eps);"),
+    "rmsnorm_no_eps": ("const double rms = sqrt(sq / (double)n + eps);", "const double rms = sqrt(sq / (double)n);"),
+    "rmsnorm_gate_sign": ("(zz / (1.0 + exp(-zz)))", "(zz / (1.0 + exp(zz)))"),
+    "rmsnorm_no_weight": ("y[r * n + j] = weight[j] * (o[r * n + j] / rms)", "y[r * n + j] = (o[r * n + j] / rms)"),
 }
 
 
