@@ -780,8 +780,11 @@ struct ChunkWs {
 
 }  // namespace
 
+// The WY inverse (I + A)^-1 is well conditioned for unit-norm keys (|A| entries
+// <= beta < 1); without the L2 norm they grow with |k|^2, so that case is left to
+// the resident form.
 bool prefill_chunked_supported(const Geom& g) {
-    if (g.dk != kDK || g.dv % kNS != 0 || g.dv > kMaxDV || g.K > kKC || g.f > kMaxF) return false;
+    if (g.dk != kDK || g.dv % kNS != 0 || g.dv > kMaxDV || g.K > kKC || g.f > kMaxF || !g.use_l2) return false;
     const size_t prep = g.io_bf16 ? PrepSmem<__nv_bfloat16>::total(g.f) : PrepSmem<float>::total(g.f);
     return prep + 1024 <= 227 * 1024;
 }

@@ -218,3 +218,27 @@ def test_prefill_empty_is_noop():
                            conv, S, z, gb.GDN_PREFILL_RESIDENT, None)
     torch.cuda.synchronize()
     assert bool((S == 1).all())
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_prefill_resident_without_l2norm(io):
+    """use_qk_l2norm = 0: only the 1/sqrt(d_k) scale; short sequences keep the un-normalised
+    recurrence (|k|^2 of tens) within fp32 range."""
+    dev = device()
+    shape = synth.Shape(2, 4, 64, 32, 4)
+    cfg, ocfg = configs(shape, io, use_l2=False)
+    x = synth.varlen_prefill(seed=95, shape=shape, lengths=[3, 0, 6, 1])
+    d = _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_RESIDENT, io)
+    o_r, c_r, S_r = _oracle_prefill(ocfg, x)
+    torch.cuda.synchronize()
+    assert_parity(f64(d["out"]), o_r, f64(d["S"]), S_r, what="resident, no L2 norm")
+
+
+def test_prefill_chunked_requires_l2norm():
+    dev = device()
+    shape = synth.Shape(2, 4, 128, 64, 4)
+    cfg, _ = configs(shape, "bf16", use_l2=False)
+    x = synth.varlen_prefill(seed=96, shape=shape, lengths=[10])
+    with pytest.raises(gb.GdnError) as e:
+        _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_CHUNKED, "bf16")
+    assert e.value.status == 8

@@ -103,3 +103,25 @@ def test_verify_block_lengths(L):
     torch.cuda.synchronize()
     assert_parity(f64(out), o_r, f64(ssnap[:, -1]), ss_r[:, -1], what=f"L={L}")
     assert np.array_equal(f64(csnap), cs_r)
+
+
+def test_verify_without_l2norm_stream_kernel():
+    """use_qk_l2norm = 0 on the streaming kernel's shape (d = 128), L = 2: outputs and
+    snapshots against the oracle."""
+    dev = device()
+    shape = synth.Shape(2, 4, 128, 128, 4)
+    cfg, ocfg = configs(shape, "bf16", use_l2=False)
+    B, L = 3, 2
+    v = synth.verify_block(97, B, L, shape)
+    H, dk, dv, D = shape.num_v_heads, shape.head_k_dim, shape.head_v_dim, shape.D
+    csnap = torch.empty(B, L, D, 3, dtype=torch.bfloat16, device=dev)
+    ssnap = torch.empty(B, L, H, dk, dv, device=dev)
+    out = torch.empty(B, L, H, dv, device=dev)
+    gb.gdn_forward_verify(cfg, B, L, to_dev(v["qkv"], dev), to_dev(v["conv_weight"], dev), to_dev(v["gate"], dev),
+                          to_dev(v["beta"], dev), to_dev(v["conv_state"], dev), to_dev(v["ssm_state"], dev), csnap,
+                          ssnap, out)
+    o_r, cs_r, ss_r = oracle.verify(ocfg, f64(v["qkv"]), f64(v["conv_weight"]), v["gate"], v["beta"],
+                                    f64(v["conv_state"]), v["ssm_state"])
+    torch.cuda.synchronize()
+    for t in range(L):
+        assert_parity(f64(out[:, t]), o_r[:, t], f64(ssnap[:, t]), ss_r[:, t], what=f"snapshot {t}")
