@@ -217,6 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
         s_pabort = 0;
     }
     __syncthreads();
+    // Programmatic dependent launch: the next launch on the stream may place its CTAs
+    // as soon as SMs free up; each launch waits here, before its first global access,
+    // for the previous one (which wrote the states this one reads) to complete.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     if (warp == kProducerWarp) {
         // ---- producer: keep the ring nstage tiles ahead ----
@@ -468,9 +473,17 @@ cudaError_t launch_t(const StepArgs& a, const GateParams& gp, const NormParams& 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int nitems = a.B * a.g.Hk;
-    const int grid = std::min(nitems, sm_count());
-    kern<<<grid, kThreads, smem, stream>>>(a, nstage, gp, np);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(nitems, sm_count()));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, nstage, gp, np);
 }
 
 }  // namespace
