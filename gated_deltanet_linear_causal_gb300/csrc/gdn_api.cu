@@ -1,6 +1,7 @@
 // gdn_api.cu -- the C ABI declared in include/gdn.h: argument validation on
-// the host, then kernel launches on the caller's stream.  No entry point
-// allocates, synchronises or copies on the host.
+// the host, then kernel launches on the caller's stream.  No compute entry point
+// allocates, synchronises or copies on the host (gdn_device_error, a diagnostic,
+// is the one synchronous call).
 #include <cmath>
 #include <cstdint>
 

@@ -17,11 +17,14 @@
 //   compute (8 warps)  runs Step 5, the gated delta rule, on each tile held in
 //                      registers, one token at a time, and stores the new state
 //                      (decode, in place) or every per-token snapshot (verify)
-//                      straight from registers.
+//                      straight from registers; with the gated RMSNorm fused
+//                      (decode, dv = 128) it writes the normalised output instead.
 // Every byte of state is read from HBM once and written once per token written.
 // Compute thread (warp w, lane l) holds columns 4l..4l+3 of rows w + 8m; the
 // reductions over dk go through shared memory in a fixed order, so decode and
 // verify produce identical bits for identical inputs.  Every wait is bounded.
+// Consecutive launches overlap through programmatic dependent launch: a launch
+// waits (griddepcontrol.wait) for the previous one before any global access.
 #include <algorithm>
 
 #include "gdn_common.cuh"

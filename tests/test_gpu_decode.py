@@ -69,3 +69,42 @@ def test_decode_batch_zero_is_noop():
     dev = device()
     cfg, _ = configs(synth.ORACLE_SCALE, "f32")
     gb.gdn_forward_decode(cfg, 0, *[torch.empty(16, device=dev)] * 7)
+
+
+def test_decode_back_to_back_launches():
+    """Consecutive decode steps launched without any host synchronisation on the same state
+    buffers (the streaming kernel overlaps consecutive launches and must still read each
+    step's states only after the previous step has written them), with a verify call in the
+    middle reading the live states; everything against the oracle at the end."""
+    dev = device()
+    shape, B, steps = synth.PRODUCTION, 8, 12
+    cfg, ocfg = configs(shape, "bf16")
+    st = synth.decode_state(98, B, shape)
+    w = to_dev(st["conv_weight"], dev)
+    conv_d, S_d = to_dev(st["conv_state"], dev), to_dev(st["ssm_state"], dev)
+    xs = [synth.decode_step(98, s, B, shape) for s in range(steps)]
+    qkv = [to_dev(x["qkv"], dev) for x in xs]
+    g = [to_dev(x["gate"], dev) for x in xs]
+    b = [to_dev(x["beta"], dev) for x in xs]
+    outs = [torch.empty(B, shape.num_v_heads, shape.head_v_dim, device=dev) for _ in range(steps)]
+    half = steps // 2
+    H, dk, dv, D = shape.num_v_heads, shape.head_k_dim, shape.head_v_dim, shape.D
+    csnap = torch.empty(B, 1, D, 3, dtype=torch.bfloat16, device=dev)
+    ssnap = torch.empty(B, 1, H, dk, dv, device=dev)
+    vout = torch.empty(B, 1, H, dv, device=dev)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        if s == half:  # verify one token of step `half` from the live states, between two decodes
+            gb.gdn_forward_verify(cfg, B, 1, qkv[s].view(B, D, 1), w, g[s].view(B, 1, H), b[s].view(B, 1, H),
+                                  conv_d, S_d, csnap, ssnap, vout)
+        gb.gdn_forward_decode(cfg, B, qkv[s], w, g[s], b[s], conv_d, S_d, outs[s])
+    torch.cuda.synchronize()
+    conv_r, S_r = f64(st["conv_state"]), st["ssm_state"].astype(np.float64)
+    for s in range(steps):
+        o_r, conv_r, S_r = oracle.decode(ocfg, f64(xs[s]["qkv"]), f64(st["conv_weight"]), xs[s]["gate"],
+                                         xs[s]["beta"], conv_r, S_r)
+        assert_parity(f64(outs[s]), o_r, what=f"step {s}")
+        if s == half:
+            assert_parity(f64(vout[:, 0]), o_r, f64(ssnap[:, 0]), S_r, what="verify between decodes")
+    assert_parity(f64(outs[-1]), o_r, f64(S_d), S_r, what="final")
+    assert np.array_equal(f64(conv_d), conv_r)
