@@ -353,7 +353,7 @@ def run_decode_gated(dev, st, steps, n_steps=128):
     return res
 
 
-def run_prefill(dev, x, variant, reps=5):
+def run_prefill(dev, x, variant, reps=20):
     import numpy as np
     import torch
     from gated_deltanet_linear_causal_gb300 import binding as gb, synth
@@ -384,7 +384,7 @@ def run_prefill(dev, x, variant, reps=5):
     return med, times
 
 
-def run_verify(dev, x, reps=10):
+def run_verify(dev, x, reps=20):
     import torch
     from gated_deltanet_linear_causal_gb300 import binding as gb
     shape = x["shape"]
@@ -404,9 +404,29 @@ def run_verify(dev, x, reps=10):
         gb.gdn_verify_commit(cfg, B, L, d["accepted"], csnap, ssnap, d["conv_state"], d["ssm_state"])
 
     verify()
-    mv, _ = _time_calls(verify, reps, lambda: scratch.zero_())
+    mv, tv = _time_calls(verify, reps, lambda: scratch.zero_())
     mc, _ = _time_calls(commit, reps, lambda: (verify(), scratch.zero_()))
-    return mv, mc
+    return mv, mc, tv
+
+
+def _env(dev):
+    """The device and software the numbers were taken on."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    env = {"gpu": p.name, "sm": f"sm_{p.major}{p.minor}", "sms": p.multi_processor_count,
+           "torch": torch.__version__, "cuda_runtime": torch.version.cuda, "driver": None}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader", "-i",
+                              str(dev.index)], capture_output=True, text=True, timeout=10)
+        env["driver"] = out.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return env
+
+
+def _spread(times):
+    """Relative spread of the repetitions: max / min - 1."""
+    return round(max(times) / min(times) - 1.0, 4)
 
 
 # ---------------------------------------------------------------------------
@@ -484,14 +504,14 @@ def main():
             med, times = run_prefill(dev, x_long, variant)
             nb = prefill_bytes(shape, x_long["cu_seqlens"], False)
             sec["prefill_L8192" + key] = {"variant": name, "tokens_per_s": round(8192 / (med / 1e3), 1),
-                                          "ms": round(med, 4),
+                                          "ms": round(med, 4), "reps": len(times), "spread": _spread(times),
                                           "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                           "algorithmic_bytes": nb, "cold_l2": True}
-            med, _ = run_prefill(dev, x_var, variant)
+            med, times = run_prefill(dev, x_var, variant)
             T = int(x_var["cu_seqlens"][-1])
             nb = prefill_bytes(shape, x_var["cu_seqlens"], True)
             sec["prefill_varlen16" + key] = {"variant": name, "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
-                                             "ms": round(med, 4),
+                                             "ms": round(med, 4), "reps": len(times), "spread": _spread(times),
                                              "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                              "algorithmic_bytes": nb, "cold_l2": True}
         ms = run_decode_raw_gates(dev, st, steps)
@@ -506,9 +526,10 @@ def main():
                                         "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                         "algorithmic_bytes": nb, "ms_decode_then_norm_kernel": round(ms_unfused, 5),
                                         "note": "gated RMSNorm fused: bf16 z in, bf16 y out"}
-        mv, mc = run_verify(dev, x_ver)
+        mv, mc, tv = run_verify(dev, x_ver)
         nb = verify_bytes(shape, 32, 4)
-        sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4),
+        sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4), "reps": len(tv),
+                                "spread": _spread(tv),
                                 "roofline_frac": round(nb / (mv / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                                 "algorithmic_bytes": nb, "commit_ms": round(mc, 4), "cold_l2": True}
     clk = clocks.stop()
@@ -531,7 +552,7 @@ def main():
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": _traffic("decode_b64", sources),
                      "kernel": "stream_kernel<bf16,128,in_place>", "algorithmic_bytes_per_launch": dec["bytes"],
                      "launch_us": round(dec["launch_us"], 2), "peak_source": peaks["source"]},
-        "e2e": dec["e2e"], "gpu_launches": args.steps, "clocks": clk,
+        "e2e": dec["e2e"], "gpu_launches": args.steps, "clocks": clk, "env": _env(dev),
     }
     if world == 1 and args.cpu_budget > 0:
         v, sample = oracle_decode_rate(dec["inputs"]["steps"], dec["inputs"]["state"], args.cpu_budget, args.steps)
