@@ -53,10 +53,23 @@ constexpr uint32_t kPBytes = kC * 2 * kC * 2;     // split [64][2*64] image: 16 
 constexpr uint32_t kWQBytes = 2 * kImgBytes;      // W and Q~ of a (chunk, value head)
 constexpr uint32_t kKPBytes = kImgBytes + kPBytes;  // K~ and P of a (chunk, value head)
 constexpr uint32_t kUSlice = kC * kNS * 4;        // fp32 u rows of one chain CTA: 8 KB
-// raw-input row: 128 channels + pad; 16-byte rows that start 4 banks apart
+// Raw inputs of one chunk are staged channel-major: one row per channel holding the
+// chunk's K-1 + 64 positions, copied from qkv in 16-byte pieces that start on a
+// 16-byte boundary of the tensor.  A row is `lead` elements of room for the
+// carried conv state, then `pieces` copies of `vec` elements; position p of
+// channel c sits at rows[c * row + dcol[c] + (p - (t0 - (K-1)))].  bf16 keeps two
+// such buffers (the next channel block is copied while the current one is
+// convolved); fp32 rows are twice as wide and keep one.
 template <typename T>
-struct RawW {
-    static constexpr int value = sizeof(T) == 2 ? kMaxDV + 8 : kMaxDV + 4;
+struct RawCfg {
+    static constexpr int vec = 16 / (int)sizeof(T);           // elements per 16-byte piece
+    static constexpr int lead = vec;                            // >= kKC - 1, a whole piece
+    static constexpr int pieces = (kC + kKC - 1 + vec - 1 + vec - 1) / vec;
+    static constexpr int row = lead + pieces * vec;             // elements per channel row
+    static constexpr int bufs = sizeof(T) == 2 ? 2 : 1;
+    static constexpr size_t rows_bytes = (size_t)kMaxDV * row * sizeof(T);
+    static constexpr size_t w_bytes = (size_t)kMaxDV * kKC * sizeof(T);
+    static constexpr size_t buf_bytes = rows_bytes + w_bytes + kMaxDV * 4;  // rows, weights, dcol
 };
 constexpr int kLd = kC + 1;                       // padded fp32 [64][65] matrices
 constexpr int kAld = kC + 4;                      // fp32 [64][68] A: 16-byte rows
@@ -116,10 +129,8 @@ struct PrepSmem {
     static constexpr size_t qk = kk + kC * kLd * 4;                // fp32 Q K^T [64][65]
     static constexpr size_t ab = qk + kC * kLd * 4;                // fp32 A [64][68]
     static constexpr size_t tb = ab + kC * kAld * 4;               // fp32 T [64][65]
-    static constexpr size_t raw = tb + kC * kLd * 4;               // raw inputs [64+K-1][RawW]
-    static constexpr size_t raw_bytes = ((size_t)(kC + kKC - 1) * RawW<T>::value * sizeof(T) + 15) & ~(size_t)15;
-    static constexpr size_t wv = raw + raw_bytes;                  // fp32 conv weights [128][kKC]
-    static constexpr size_t nrm = wv + kMaxDV * kKC * 4;           // fp32 partial sums of squares [8][64]
+    static constexpr size_t raw = tb + kC * kLd * 4;               // RawCfg<T>::bufs raw-input buffers
+    static constexpr size_t nrm = raw + RawCfg<T>::bufs * RawCfg<T>::buf_bytes;  // fp32 partial sums of squares [8][64]
     static constexpr size_t gates = nrm + 8 * kC * 4;              // fp32 G, gamma, c, beta [f][64] each
     static size_t total(int f) { return gates + (size_t)4 * f * kC * 4; }
 };
@@ -138,83 +149,93 @@ struct ChunkOut {
 // against the oracle's tolerance, not bit for bit against the decode path.
 __device__ __forceinline__ float silu_fast(float y) { return __fmul_rn(y, __frcp_rn(__fadd_rn(1.f, __expf(-y)))); }
 
-// Raw inputs of channels chan(i), i < nch, at positions t0-(K-1) .. t0+63 into
-// raw[r][i] (r = position - t0 + K-1): from qkv inside the sequence, from the
-// carried conv state before its start, 0 past the chunk's last token.  Warps
-// w0 .. w0+nw-1, one channel row per warp (lanes along positions, coalesced),
-// kU rows in flight.
-template <typename T, int kU, typename Chan>
-__device__ __forceinline__ void load_raw(const PrefillArgs& a, T* raw, int nch, Chan chan, int n, int tb, int t0,
-                                         int cnt, int w0, int nw) {
-    constexpr int W = RawW<T>::value;
-    const Geom& g = a.g;
-    const int K = g.K, warp = (threadIdx.x >> 5) - w0, lane = threadIdx.x & 31;
-    const T* qkv = static_cast<const T*>(a.qkv);
-    const T* cst = static_cast<const T*>(a.conv_state);
-    constexpr int kRows = (kC + kKC - 1 + 31) / 32;
-    for (int i0 = kU * warp; i0 < nch; i0 += kU * nw) {
-        T v[kU][kRows];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int i = i0 + u;
-            const int c = i < nch ? chan(i) : 0;
-#pragma unroll
-            for (int q = 0; q < kRows; ++q) {
-                const int r = lane + 32 * q, j = r - (K - 1), p = t0 + j;
-                v[u][q] = zero_elem<T>();
-                if (i < nch && r < kC + K - 1 && j < cnt)
-                    v[u][q] = p >= tb ? qkv[(size_t)c * a.T + p] : cst[((size_t)n * g.D + c) * (K - 1) + (p - tb + K - 1)];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-#pragma unroll
-            for (int q = 0; q < kRows; ++q) {
-                const int r = lane + 32 * q;
-                if (i0 + u < nch && r < kC + K - 1) raw[r * W + i0 + u] = v[u][q];
-            }
-    }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-// Eight consecutive channels c..c+7 of raw row r as fp32.
-__device__ __forceinline__ void raw8(const __nv_bfloat16* raw, int r, int c, float (&x)[8]) {
-    const uint4 b = *reinterpret_cast<const uint4*>(raw + r * RawW<__nv_bfloat16>::value + c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h[e]);
-        x[2 * e] = f.x;
-        x[2 * e + 1] = f.y;
-    }
-}
-__device__ __forceinline__ void raw8(const float* raw, int r, int c, float (&x)[8]) {
-    const float4 lo = *reinterpret_cast<const float4*>(raw + r * RawW<float>::value + c);
-    const float4 hi = *reinterpret_cast<const float4*>(raw + r * RawW<float>::value + c + 4);
-    x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
-    x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
-}
-
-// Depthwise causal conv + SiLU of channels c..c+7 at chunk token t (raw rows
-// t .. t+K-1, newest last); weights wv[channel][kKC].
+// One raw-input buffer: channel rows, the channels' conv weights and their row offsets.
 template <typename T>
-__device__ __forceinline__ void conv8(const T* raw, const float* wv, int t, int c, int K, float (&y)[8]) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float4 wt[8];
+struct RawBuf {
+    T* rows;
+    T* w;
+    int* dcol;
+    __device__ RawBuf(unsigned char* base)
+        : rows(reinterpret_cast<T*>(base)),
+          w(reinterpret_cast<T*>(base + RawCfg<T>::rows_bytes)),
+          dcol(reinterpret_cast<int*>(base + RawCfg<T>::rows_bytes + RawCfg<T>::w_bytes)) {}
+};
+
+// Start copying channels cb .. cb+nch-1 of the chunk (positions t0-(K-1) .. t0+63,
+// from the sequence start tb on) and their conv weights into buffer rb, by threads
+// ti = 0 .. nt-1 of the caller's group; one cp.async group per thread.  Pieces
+// past the end of qkv are skipped (D is a multiple of 8, so a piece that starts
+// inside the tensor ends inside it); positions before tb are filled by
+// fill_conv_state once the copies have landed.
+template <typename T>
+__device__ __forceinline__ void issue_raw(const PrefillArgs& a, const RawBuf<T>& rb, int cb, int nch, int tb, int t0,
+                                          int ti, int nt) {
+    using R = RawCfg<T>;
+    const Geom& g = a.g;
+    const int K = g.K, p0 = t0 - (K - 1), pf = max(p0, tb);
+    const T* qkv = static_cast<const T*>(a.qkv);
+    const long long total = (long long)g.D * a.T;
+    for (int idx = ti; idx < nch * R::pieces; idx += nt) {
+        const int c = idx / R::pieces, k = idx - c * R::pieces;
+        const long long e = (long long)(cb + c) * a.T + pf;
+        const long long A = e & ~(long long)(R::vec - 1);
+        if (k == 0) rb.dcol[c] = R::lead + (int)(e - A) - (pf - p0);
+        const long long E = A + (long long)k * R::vec;
+        if (E < total) cp_async16(rb.rows + c * R::row + R::lead + k * R::vec, qkv + E);
+    }
+    const T* w = static_cast<const T*>(a.w) + (size_t)cb * K;
+    if ((reinterpret_cast<uintptr_t>(w) & 15) == 0) {  // nch * K * sizeof(T) is a multiple of 16 here
+        for (int idx = ti; idx < nch * K * (int)sizeof(T) / 16; idx += nt)
+            cp_async16(reinterpret_cast<unsigned char*>(rb.w) + 16 * idx, reinterpret_cast<const unsigned char*>(w) + 16 * idx);
+    } else {
+        for (int idx = ti; idx < nch * K; idx += nt) rb.w[idx] = w[idx];
+    }
+    cp_async_commit();
+}
+
+// Positions t0-(K-1) .. tb-1 of the sequence's first chunk come from the carried
+// conv state (after the copies into rb have landed and are visible).
+template <typename T>
+__device__ __forceinline__ void fill_conv_state(const PrefillArgs& a, const RawBuf<T>& rb, int cb, int nch, int n, int tb,
+                                                int t0, int ti, int nt) {
+    const Geom& g = a.g;
+    const int K = g.K, p0 = t0 - (K - 1), np = tb - p0;
+    const T* cst = static_cast<const T*>(a.conv_state);
+    for (int idx = ti; idx < nch * np; idx += nt) {
+        const int c = idx / np, i = idx - c * np;
+        rb.rows[c * RawCfg<T>::row + rb.dcol[c] + i] = cst[((size_t)n * g.D + cb + c) * (K - 1) + (i - np + K - 1)];
+    }
+}
+
+// The K taps of a channel's conv weights as fp32 (0 past K).
+template <typename T>
+__device__ __forceinline__ void taps(const T* wc, int K, float (&w)[kKC]) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) wt[e] = *reinterpret_cast<const float4*>(wv + (c + e) * kKC);
+    for (int tap = 0; tap < kKC; ++tap) w[tap] = tap < K ? to_f32(wc[tap]) : 0.f;
+}
+
+// Depthwise causal conv + SiLU of channels c..c+7 of buffer rb at chunk token t
+// (positions t .. t+K-1 of the rows, newest last).
+template <typename T>
+__device__ __forceinline__ void conv8(const RawBuf<T>& rb, int t, int c, int K, float (&y)[8]) {
 #pragma unroll
-    for (int tap = 0; tap < kKC; ++tap)
-        if (tap < K) {
-            float x[8];
-            raw8(raw, t + tap, c, x);
+    for (int e = 0; e < 8; ++e) {
+        float w[kKC];
+        taps(rb.w + (c + e) * K, K, w);
+        const T* x = rb.rows + (c + e) * RawCfg<T>::row + rb.dcol[c + e] + t;
+        float acc = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float wk = tap == 0 ? wt[e].x : tap == 1 ? wt[e].y : tap == 2 ? wt[e].z : wt[e].w;
-                acc[e] = fmaf(wk, x[e], acc[e]);
-            }
-        }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = silu_fast(acc[e]);
+        for (int tap = 0; tap < kKC; ++tap)
+            if (tap < K) acc = fmaf(w[tap], to_f32(x[tap]), acc);
+        y[e] = silu_fast(acc);
+    }
 }
 
 // T = (I + A)^-1 for strictly lower A (row stride kAld) into Tb (row stride kLd),
@@ -303,8 +324,8 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     float* qk = reinterpret_cast<float*>(smem + L::qk);
     float* Ab = reinterpret_cast<float*>(smem + L::ab);
     float* Tb = reinterpret_cast<float*>(smem + L::tb);
-    T* raw = reinterpret_cast<T*>(smem + L::raw);
-    float* wv = reinterpret_cast<float*>(smem + L::wv);
+    using R = RawCfg<T>;
+    auto rbuf = [&](int b) { return RawBuf<T>(smem + L::raw + (size_t)b * R::buf_bytes); };
     float* nrm = reinterpret_cast<float*>(smem + L::nrm);
     const Geom& g = a.g;
     const int f = g.f;
@@ -322,7 +343,13 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     const int t0 = tb + (chunk - coff[n]) * kC;
     const int cnt = min(kC, a.cu[n + 1] - t0);
     const int K = g.K;
-    const T* w = static_cast<const T*>(a.w);
+    const bool first = t0 - (K - 1) < tb;  // the conv window reaches into the carried conv state
+    constexpr int kBarV = 1, kBarT = 2, kGrp = kPT / 2;  // warps 8-15: V; warps 0-7: A, T
+    const int cbq = hk * kDK, cbk = (g.Hk + hk) * kDK;
+    auto cbv = [&](int j) { return 2 * g.Hk * kDK + (hk * f + j) * g.dv; };
+    // raw inputs of Q (and, with two buffers, of K) start copying at once
+    issue_raw<T>(a, rbuf(0), cbq, kDK, tb, t0, tid, kPT);
+    if (R::bufs == 2) issue_raw<T>(a, rbuf(1), cbk, kDK, tb, t0, tid, kPT);
     if (warp == 0) umma::tmem_alloc(&s_tmem, 512);
     if (tid == 0) {
         mbar_init(&s_bar, 1);
@@ -341,13 +368,18 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     // thread (t, part): token t = tid % 64, channels 16*part .. +15 of the head;
     // lanes run along tokens, so operand-image rows are written 16 bytes apart
     for (int pass = 0; pass < 2; ++pass) {
-        const int cb = pass == 0 ? hk * kDK : g.Hk * kDK + hk * kDK;
-        load_raw<T, 8>(a, raw, kDK, [&](int i) { return cb + i; }, n, tb, t0, cnt, 0, kPT / 32);
-        for (int idx = tid; idx < kDK * kKC; idx += kPT) {
-            const int c = idx / kKC, tap = idx - c * kKC;
-            wv[idx] = tap < K ? to_f32(w[(size_t)(cb + c) * K + tap]) : 0.f;
-        }
+        const int cb = pass == 0 ? cbq : cbk;
+        const RawBuf<T> rb = rbuf(R::bufs == 2 ? pass : 0);
+        if (R::bufs == 1 && pass == 1) issue_raw<T>(a, rb, cbk, kDK, tb, t0, tid, kPT);
+        // pending groups newer than this pass's: K during pass 0, and V0 (value-head
+        // warps) during pass 1, with two buffers
+        if (R::bufs == 2 && (pass == 0 || tid >= kGrp)) cp_async_wait<1>();
+        else cp_async_wait<0>();
         __syncthreads();
+        if (first) {
+            fill_conv_state<T>(a, rb, cb, kDK, n, tb, t0, tid, kPT);
+            __syncthreads();
+        }
         if (pass == 0) {
             scan_heads(sG, f);
             for (int idx = tid; idx < f * kC; idx += kPT) {
@@ -364,7 +396,7 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
             float y[8];
-            conv8(raw, wv, t, 16 * part + 8 * gi, K, y);
+            conv8(rb, t, 16 * part + 8 * gi, K, y);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 v[8 * gi + e] = y[e];
@@ -394,7 +426,9 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
             umma::store_split8(dst, t, 16 * part, kDK, sv);
             umma::store_split8(dst, t, 16 * part + 8, kDK, sv + 8);
         }
-        __syncthreads();  // raw inputs, weights and partial sums are reused by the next pass
+        __syncthreads();  // the partial sums are reused by the next pass; the raw buffer is free
+        // with two buffers, value head `pass` starts copying into the buffer just freed
+        if (R::bufs == 2 && tid >= kGrp && pass < f) issue_raw<T>(a, rb, cbv(pass), g.dv, tb, t0, tid - kGrp, kGrp);
     }
 
     // ---- [K; Q] K^T on the tensor cores: rows 0-63 K K^T, rows 64-127 Q K^T ----
@@ -411,7 +445,6 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     uint32_t phase = 0;
     const uint32_t wl = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
     const int row = 16 * (warp & 3) + (lane & 15);          // M = 64 rows sit in lanes 0-15 of each quarter
-    constexpr int kBarV = 1, kBarT = 2, kGrp = kPT / 2;     // warps 8-15: V; warps 0-7: A, T
     for (int j = 0; j < f; ++j) {
         const int h = hk * f + j;
         const size_t rec = (size_t)chunk * g.Hv + h;
@@ -461,24 +494,30 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                 umma::store_split8(timg + kPBytes, t, s0, kC, tbt);
             }
         } else {
-            // ---- V: raw inputs, weights, conv + SiLU into the V image ----
-            const int cv = 2 * g.Hk * kDK + h * g.dv;  // first V channel of the head
+            // ---- V: conv + SiLU of the head's raw inputs into the V image ----
             const int vt = tid - kGrp;
-            load_raw<T, 16>(a, raw, g.dv, [&](int i) { return cv + i; }, n, tb, t0, cnt, 8, 8);
-            for (int idx = vt; idx < g.dv * kKC; idx += kGrp) {
-                const int c = idx / kKC, tap = idx - c * kKC;
-                wv[idx] = tap < K ? to_f32(w[(size_t)(cv + c) * K + tap]) : 0.f;
-            }
+            const RawBuf<T> rb = rbuf(R::bufs == 2 ? (j & 1) : 0);
+            if (R::bufs == 1) issue_raw<T>(a, rb, cbv(j), g.dv, tb, t0, vt, kGrp);
+            if (R::bufs == 2 && j + 1 < f) cp_async_wait<1>();  // value head j+1 may still be copying
+            else cp_async_wait<0>();
             if (j == 0 && !mbar_wait_bounded(&s_bar, 0)) s_fail = 1;  // the Q image is free once the Gram products are done
             named_sync(kBarV, kGrp);
+            if (first) {
+                fill_conv_state<T>(a, rb, cbv(j), g.dv, n, tb, t0, vt, kGrp);
+                named_sync(kBarV, kGrp);
+            }
             for (int idx = vt; idx < kC * (g.dv / 8); idx += kGrp) {
                 const int t = idx & (kC - 1), c = 8 * (idx >> 6);
                 float y[8];
-                conv8(raw, wv, t, c, K, y);
+                conv8(rb, t, c, K, y);
                 if (t >= cnt)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) y[e] = 0.f;
                 umma::store_split8(qimg, t, c, g.dv, y);
+            }
+            if (R::bufs == 2 && j + 2 < f) {  // the buffer is free: value head j+2 starts copying
+                named_sync(kBarV, kGrp);
+                issue_raw<T>(a, rb, cbv(j + 2), g.dv, tb, t0, vt, kGrp);
             }
         }
         if (j == 0 && !s_fail) phase ^= 1;
@@ -527,6 +566,7 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
         flag_device_error(&g_chunk_error, 7);
         mbar_wait_bounded(&s_bar, phase);  // give the MMAs a last chance to land before TMEM is freed
     }
+    cp_async_wait<0>();  // after an early exit, copies issued for later value heads may still be landing
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 512);
