@@ -72,7 +72,7 @@ struct RawCfg {
     static constexpr size_t buf_bytes = rows_bytes + w_bytes + kMaxDV * 4;  // rows, weights, dcol
 };
 constexpr int kLd = kC + 1;                       // padded fp32 [64][65] matrices
-constexpr int kAld = kC + 4;                      // fp32 [64][68] A: 16-byte rows
+constexpr int kAld = kC + 4;                      // fp32 [64][68] A and T: 16-byte rows
 
 // Chunk offsets: coff[n] = number of chunks of the sequences before n.
 __global__ void plan_kernel(const int32_t* __restrict__ cu, int N, int32_t* __restrict__ coff) {
@@ -128,8 +128,8 @@ struct PrepSmem {
     static constexpr size_t kk = timg + 2 * kPBytes;               // fp32 K K^T [64][65]
     static constexpr size_t qk = kk + kC * kLd * 4;                // fp32 Q K^T [64][65]
     static constexpr size_t ab = qk + kC * kLd * 4;                // fp32 A [64][68]
-    static constexpr size_t tb = ab + kC * kAld * 4;               // fp32 T [64][65]
-    static constexpr size_t raw = tb + kC * kLd * 4;               // RawCfg<T>::bufs raw-input buffers
+    static constexpr size_t tb = ab + kC * kAld * 4;               // fp32 T [64][68]
+    static constexpr size_t raw = tb + kC * kAld * 4;              // RawCfg<T>::bufs raw-input buffers
     static constexpr size_t nrm = raw + RawCfg<T>::bufs * RawCfg<T>::buf_bytes;  // fp32 partial sums of squares [8][64]
     static constexpr size_t gates = nrm + 8 * kC * 4;              // fp32 G, gamma, c, beta [f][64] each
     static size_t total(int f) { return gates + (size_t)4 * f * kC * 4; }
@@ -238,14 +238,17 @@ __device__ __forceinline__ void conv8(const RawBuf<T>& rb, int t, int c, int K, 
     }
 }
 
-// T = (I + A)^-1 for strictly lower A (row stride kAld) into Tb (row stride kLd),
-// by the 256 threads of one group (named barrier `bar`), blocked:
+// T = (I + A)^-1 for strictly lower A into Tb (both row stride kAld, 16-byte
+// rows), by the 256 threads of one group (named barrier `bar`), blocked:
 //   the four 16x16 diagonal blocks by forward substitution, one thread per
 //   column (T[i][u] = -sum_{u<=s<i} A[i][s] T[s][u], T[u][u] = 1);
 //   then for block size B = 16 (two pairs) and B = 32 (one pair) the block
 //   below the diagonal, T21 = -T22 (A21 T11), via scratch X = A21 T11 (the
 //   sums run over whole blocks: the stored zeros of the triangular factors
-//   drop out).
+//   drop out).  Row operands are read four at a time; every sum runs in order
+//   of its index.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
 __device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float* X, int gt, int bar) {
     constexpr int kG = kPT / 2;
     if (gt < kC) {
@@ -257,11 +260,11 @@ __device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float
 #pragma unroll
             for (int s = 0; s < i; ++s) acc = fmaf(A[(o + i) * kAld + o + s], tc[s], acc);
             tc[i] = i < u ? 0.f : i == u ? 1.f : -acc;
-            Tb[(o + i) * kLd + o + u] = tc[i];
+            Tb[(o + i) * kAld + o + u] = tc[i];
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i)  // the rest of the block row right of the diagonal block
-            for (int jb = o + 16; jb < kC; jb += 16) Tb[(o + i) * kLd + jb + u] = 0.f;
+            for (int jb = o + 16; jb < kC; jb += 16) Tb[(o + i) * kAld + jb + u] = 0.f;
     }
     named_sync(bar, kG);
     // B = 16: the two pairs, element (r, c) of pair p by thread (p's share): gt -> r, c; p = 0, 1
@@ -269,21 +272,31 @@ __device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float
         const int r = gt >> 4, c = gt & 15;
         float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            x0 = fmaf(A[(16 + r) * kAld + m], Tb[m * kLd + c], x0);
-            x1 = fmaf(A[(48 + r) * kAld + 32 + m], Tb[(32 + m) * kLd + 32 + c], x1);
+        for (int m = 0; m < 16; m += 4) {
+            const float4 a0 = ld4(A + (16 + r) * kAld + m), a1 = ld4(A + (48 + r) * kAld + 32 + m);
+            const float* t0 = Tb + m * kAld + c;
+            const float* t1 = Tb + (32 + m) * kAld + 32 + c;
+            x0 = fmaf(a0.x, t0[0], x0); x0 = fmaf(a0.y, t0[kAld], x0);
+            x0 = fmaf(a0.z, t0[2 * kAld], x0); x0 = fmaf(a0.w, t0[3 * kAld], x0);
+            x1 = fmaf(a1.x, t1[0], x1); x1 = fmaf(a1.y, t1[kAld], x1);
+            x1 = fmaf(a1.z, t1[2 * kAld], x1); x1 = fmaf(a1.w, t1[3 * kAld], x1);
         }
         X[gt] = x0;
         X[256 + gt] = x1;
         named_sync(bar, kG);
         float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            y0 = fmaf(Tb[(16 + r) * kLd + 16 + m], X[m * 16 + c], y0);
-            y1 = fmaf(Tb[(48 + r) * kLd + 48 + m], X[256 + m * 16 + c], y1);
+        for (int m = 0; m < 16; m += 4) {
+            const float4 b0 = ld4(Tb + (16 + r) * kAld + 16 + m), b1 = ld4(Tb + (48 + r) * kAld + 48 + m);
+            const float* z0 = X + m * 16 + c;
+            const float* z1 = X + 256 + m * 16 + c;
+            y0 = fmaf(b0.x, z0[0], y0); y0 = fmaf(b0.y, z0[16], y0);
+            y0 = fmaf(b0.z, z0[32], y0); y0 = fmaf(b0.w, z0[48], y0);
+            y1 = fmaf(b1.x, z1[0], y1); y1 = fmaf(b1.y, z1[16], y1);
+            y1 = fmaf(b1.z, z1[32], y1); y1 = fmaf(b1.w, z1[48], y1);
         }
-        Tb[(16 + r) * kLd + c] = -y0;
-        Tb[(48 + r) * kLd + 32 + c] = -y1;
+        Tb[(16 + r) * kAld + c] = -y0;
+        Tb[(48 + r) * kAld + 32 + c] = -y1;
         named_sync(bar, kG);
     }
     // B = 32: rows r, r+8, r+16, r+24 and column c of the lower-left block by each thread
@@ -291,23 +304,37 @@ __device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float
         const int r = gt >> 5, c = gt & 31;
         float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const float tm = Tb[m * kLd + c];
+        for (int m = 0; m < 32; m += 4) {
+            const float* tcol = Tb + m * kAld + c;
+            const float t0 = tcol[0], t1 = tcol[kAld], t2 = tcol[2 * kAld], t3 = tcol[3 * kAld];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) x[q] = fmaf(A[(32 + r + 8 * q) * kAld + m], tm, x[q]);
+            for (int q = 0; q < 4; ++q) {
+                const float4 av = ld4(A + (32 + r + 8 * q) * kAld + m);
+                x[q] = fmaf(av.x, t0, x[q]);
+                x[q] = fmaf(av.y, t1, x[q]);
+                x[q] = fmaf(av.z, t2, x[q]);
+                x[q] = fmaf(av.w, t3, x[q]);
+            }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) X[(r + 8 * q) * 32 + c] = x[q];
         named_sync(bar, kG);
         float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const float xm = X[m * 32 + c];
+        for (int m = 0; m < 32; m += 4) {
+            const float* xcol = X + m * 32 + c;
+            const float x0 = xcol[0], x1 = xcol[32], x2 = xcol[64], x3 = xcol[96];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) y[q] = fmaf(Tb[(32 + r + 8 * q) * kLd + 32 + m], xm, y[q]);
+            for (int q = 0; q < 4; ++q) {
+                const float4 tv = ld4(Tb + (32 + r + 8 * q) * kAld + 32 + m);
+                y[q] = fmaf(tv.x, x0, y[q]);
+                y[q] = fmaf(tv.y, x1, y[q]);
+                y[q] = fmaf(tv.z, x2, y[q]);
+                y[q] = fmaf(tv.w, x3, y[q]);
+            }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) Tb[(32 + r + 8 * q) * kLd + c] = -y[q];
+        for (int q = 0; q < 4; ++q) Tb[(32 + r + 8 * q) * kAld + c] = -y[q];
         named_sync(bar, kG);
     }
 }
@@ -467,14 +494,16 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
             unsigned char* pimg = ws.kp + rec * kKPBytes + kImgBytes;
             for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
                 const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
-                float pv[8];
+                float pv[8], av[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int s = s0 + e;
                     const float dec = s <= t ? expf(Gj[t] - Gj[s]) : 0.f;
-                    Ab[t * kAld + s] = s < t ? __fmul_rn(__fmul_rn(Bj[t], dec), kk[t * kLd + s]) : 0.f;
+                    av[e] = s < t ? __fmul_rn(__fmul_rn(Bj[t], dec), kk[t * kLd + s]) : 0.f;
                     pv[e] = __fmul_rn(dec, qk[t * kLd + s]);
                 }
+                *reinterpret_cast<float4*>(Ab + t * kAld + s0) = make_float4(av[0], av[1], av[2], av[3]);
+                *reinterpret_cast<float4*>(Ab + t * kAld + s0 + 4) = make_float4(av[4], av[5], av[6], av[7]);
                 umma::store_split8(pimg, t, s0, kC, pv);
             }
             named_sync(kBarT, kGrp);
@@ -482,11 +511,13 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
             // T diag(beta gamma) and T diag(beta) as A operands
             for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
                 const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
+                const float4 tl = ld4(Tb + t * kAld + s0), th = ld4(Tb + t * kAld + s0 + 4);
+                const float trow[8] = {tl.x, tl.y, tl.z, tl.w, th.x, th.y, th.z, th.w};
                 float tg[8], tbt[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int s = s0 + e;
-                    const float tv = Tb[t * kLd + s];
+                    const float tv = trow[e];
                     tg[e] = __fmul_rn(tv, __fmul_rn(Bj[s], Yj[s]));
                     tbt[e] = __fmul_rn(tv, Bj[s]);
                 }
