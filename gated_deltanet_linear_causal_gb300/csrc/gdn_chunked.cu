@@ -214,27 +214,80 @@ __device__ __forceinline__ void fill_conv_state(const PrefillArgs& a, const RawB
     }
 }
 
-// The K taps of a channel's conv weights as fp32 (0 past K).
-template <typename T>
-__device__ __forceinline__ void taps(const T* wc, int K, float (&w)[kKC]) {
+// Conv weights of channels c..c+7 (c % 8 == 0) as fp32, 0 past K: with K = kKC
+// they are 16-byte rows of the weight block, read a row at a time.
+__device__ __forceinline__ void bf16x8(const uint4 u, float* dst) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-    for (int tap = 0; tap < kKC; ++tap) w[tap] = tap < K ? to_f32(wc[tap]) : 0.f;
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        dst[2 * i] = f.x;
+        dst[2 * i + 1] = f.y;
+    }
+}
+template <typename T>
+__device__ __forceinline__ void taps8(const T* wb, int c, int K, float (&w)[8][kKC]) {
+    if (K == kKC) {
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) bf16x8(*reinterpret_cast<const uint4*>(wb + (c + 2 * q) * kKC), &w[2 * q][0]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 v = *reinterpret_cast<const float4*>(wb + (c + e) * kKC);
+                w[e][0] = v.x; w[e][1] = v.y; w[e][2] = v.z; w[e][3] = v.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int tap = 0; tap < kKC; ++tap) w[e][tap] = tap < K ? to_f32(wb[(c + e) * K + tap]) : 0.f;
+    }
 }
 
-// Depthwise causal conv + SiLU of channels c..c+7 of buffer rb at chunk token t
-// (positions t .. t+K-1 of the rows, newest last).
+// Depthwise causal conv + SiLU of channels c..c+7 (c % 8 == 0) of buffer rb at
+// chunk token t (positions t .. t+K-1 of the rows, newest last).
 template <typename T>
 __device__ __forceinline__ void conv8(const RawBuf<T>& rb, int t, int c, int K, float (&y)[8]) {
+    const int4 da = *reinterpret_cast<const int4*>(rb.dcol + c), db = *reinterpret_cast<const int4*>(rb.dcol + c + 4);
+    const int dc[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+    float w[8][kKC];
+    taps8(rb.w, c, K, w);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        float w[kKC];
-        taps(rb.w + (c + e) * K, K, w);
-        const T* x = rb.rows + (c + e) * RawCfg<T>::row + rb.dcol[c + e] + t;
+        const T* x = rb.rows + (c + e) * RawCfg<T>::row + dc[e] + t;
         float acc = 0.f;
 #pragma unroll
         for (int tap = 0; tap < kKC; ++tap)
-            if (tap < K) acc = fmaf(w[tap], to_f32(x[tap]), acc);
+            if (tap < K) acc = fmaf(w[e][tap], to_f32(x[tap]), acc);
         y[e] = silu_fast(acc);
+    }
+}
+
+// The same at tokens t and t+1 (positions t .. t+K of the rows): the window is
+// read once for both.
+template <typename T>
+__device__ __forceinline__ void conv8x2(const RawBuf<T>& rb, int t, int c, int K, float (&y0)[8], float (&y1)[8]) {
+    const int4 da = *reinterpret_cast<const int4*>(rb.dcol + c), db = *reinterpret_cast<const int4*>(rb.dcol + c + 4);
+    const int dc[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+    float w[8][kKC];
+    taps8(rb.w, c, K, w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const T* x = rb.rows + (c + e) * RawCfg<T>::row + dc[e] + t;
+        float xv[kKC + 1];
+#pragma unroll
+        for (int i = 0; i <= kKC; ++i) xv[i] = i <= K ? to_f32(x[i]) : 0.f;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int tap = 0; tap < kKC; ++tap)
+            if (tap < K) {
+                a0 = fmaf(w[e][tap], xv[tap], a0);
+                a1 = fmaf(w[e][tap], xv[tap + 1], a1);
+            }
+        y0[e] = silu_fast(a0);
+        y1[e] = silu_fast(a1);
     }
 }
 
@@ -537,14 +590,17 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                 fill_conv_state<T>(a, rb, cbv(j), g.dv, n, tb, t0, vt, kGrp);
                 named_sync(kBarV, kGrp);
             }
-            for (int idx = vt; idx < kC * (g.dv / 8); idx += kGrp) {
-                const int t = idx & (kC - 1), c = 8 * (idx >> 6);
-                float y[8];
-                conv8(rb, t, c, K, y);
-                if (t >= cnt)
+            for (int idx = vt; idx < (kC / 2) * (g.dv / 8); idx += kGrp) {  // lanes along token pairs
+                const int t = 2 * (idx & (kC / 2 - 1)), c = 8 * (idx >> 5);
+                float y0[8], y1[8];
+                conv8x2(rb, t, c, K, y0, y1);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = 0.f;
-                umma::store_split8(qimg, t, c, g.dv, y);
+                for (int e = 0; e < 8; ++e) {
+                    if (t >= cnt) y0[e] = 0.f;
+                    if (t + 1 >= cnt) y1[e] = 0.f;
+                }
+                umma::store_split8(qimg, t, c, g.dv, y0);
+                umma::store_split8(qimg, t + 1, c, g.dv, y1);
             }
             if (R::bufs == 2 && j + 2 < f) {  // the buffer is free: value head j+2 starts copying
                 named_sync(kBarV, kGrp);
