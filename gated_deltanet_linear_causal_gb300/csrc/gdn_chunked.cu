@@ -660,6 +660,15 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
 }
 
 // ---- chain ----------------------------------------------------------------------
+// A product accumulated by umma::mma_split_bpair: the sum of its two 32-column halves.
+__device__ __forceinline__ void tmem_pair(uint32_t taddr, float (&v)[kNS]) {
+    float w[kNS];
+    umma::tmem_ld32(taddr, v);
+    umma::tmem_ld32(taddr + kNS, w);
+#pragma unroll
+    for (int j = 0; j < kNS; ++j) v[j] = __fadd_rn(v[j], w[j]);
+}
+
 // Per chunk c (b = c & 1), with M = 128 products (a tcgen05 MMA costs the same
 // issue time at M = 64 and M = 128, so operands are stacked):
 //   round A   MMA  [W_c; Q~_c] S0 -> tA[b]: rows 0-63 X = W S0, rows 64-127 Q~ S0
@@ -721,7 +730,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 #pragma unroll
     for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
 
-    if (warp == 0) umma::tmem_alloc(&s_tmem, 128);
+    if (warp == 0) umma::tmem_alloc(&s_tmem, 256);
     if (tid == 0) {
         mbar_init(&s_wq[0], 1);
         mbar_init(&s_wq[1], 1);
@@ -739,7 +748,8 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = s_tmem;
-    const uint32_t tS = tmem, tA0 = tmem + 32;      // tA[b] = tA0 + 32 b
+    // accumulators of 2 x 32 columns (the hi*hi + lo*hi and hi*lo halves of a product)
+    const uint32_t tS = tmem, tA0 = tmem + 64;      // tA[b] = tA0 + 64 b
     const uint32_t wl = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes = accumulator rows 32 warp ..
 
     // thread 0's count of copies and MMA commits issued per barrier (for a clean exit on abort)
@@ -776,7 +786,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         wait_all(&s_o, (uint32_t)(cc & 1));
         umma::fence_after_sync();
         float ov[kNS];
-        umma::tmem_ld32(tA0 + 32 * (cc & 1) + wl, ov);
+        tmem_pair(tA0 + 64 * (cc & 1) + wl, ov);
         const int t0 = tb + cc * kC, cnt = min(kC, te - t0), t = 32 * (warp - 2) + lane;
         if (t < cnt) {
             float* orow = a.out + ((size_t)(t0 + t) * g.Hv + h) * g.dv + col0;
@@ -798,7 +808,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         // ---- round A: [W; Q~] S0 ----
         wait_all(&s_wq[b], (uint32_t)((c >> 1) & 1));
         if (tid == 0) {
-            umma::mma_split(tA0 + 32 * b, wqb + b * kWQBytes, false, s0t, true, 2 * kC, kNS, kDK, false);
+            umma::mma_split_bpair(tA0 + 64 * b, wqb + b * kWQBytes, false, s0t, 2 * kC, kNS, kDK, false);
             umma::commit(&s_a);
             ++a_iss;
             if (c > 0) {  // P U of chunk c-1 has completed: the P buffer is free
@@ -813,7 +823,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             wait_all(&s_u, (uint32_t)(c & 1));
             umma::fence_after_sync();
             float xv[kNS];
-            umma::tmem_ld32(tA0 + 32 * b + wl, xv);
+            tmem_pair(tA0 + 64 * b + wl, xv);
             const float* ur = ub + tid * kNS;
             float uu[kNS];
 #pragma unroll
@@ -837,17 +847,17 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         if (tid == 0) {
             if (c + 1 < nch) load_u(c + 1);  // the u rows of chunk c have been read (the barrier above)
             if (!mbar_wait_bounded(&s_k, (uint32_t)(c & 1))) s_abort = 1;
-            umma::mma_split(tS, kt, true, ut, true, kDK, kNS, kC, false);
+            umma::mma_split_bpair(tS, kt, true, ut, kDK, kNS, kC, false);
             umma::commit(&s_s);
             if (!mbar_wait_bounded(&s_p, (uint32_t)(c & 1))) s_abort = 1;
-            umma::mma_split(tA0 + 32 * b, pp, false, ut, true, 2 * kC, kNS, kC, true);
+            umma::mma_split_bpair(tA0 + 64 * b, pp, false, ut, 2 * kC, kNS, kC, true);
             umma::commit(&s_o);
             ++b_iss;
         }
         wait_all(&s_s, (uint32_t)(c & 1));
         umma::fence_after_sync();
         float ss[kNS];
-        umma::tmem_ld32(tS + wl, ss);
+        tmem_pair(tS + wl, ss);
 #pragma unroll
         for (int j = 0; j < kNS; ++j) S[j] = fmaf(glc, S[j], ss[j]);
 #pragma unroll
@@ -880,7 +890,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_free(tmem, 128);
+    if (warp == 0) umma::tmem_free(tmem, 256);
     if (s_abort) return;
 #pragma unroll
     for (int j = 0; j < kNS; j += 4) *reinterpret_cast<float4*>(Sg + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);

@@ -81,6 +81,29 @@ __device__ __forceinline__ void mma_split(uint32_t d_tmem, const unsigned char* 
     }
 }
 
+// The same product when B is MN-major with its hi and lo halves side by side
+// ([K rows][2N], hi in columns 0..N-1): per k-step one MMA of width 2N gives
+// [A_hi B_hi | A_hi B_lo] and one of width N adds A_lo B_hi to the first half, so
+// the product is D[:, 0:N] + D[:, N:2N] -- two instructions per k-step instead of
+// three.  D takes 2N TMEM columns.
+__device__ __forceinline__ void mma_split_bpair(uint32_t d_tmem, const unsigned char* a, bool a_mn, const unsigned char* b,
+                                                int M, int N, int K, bool accumulate) {
+    const uint32_t idesc2 = idesc_bf16(M, 2 * N, a_mn) | (1u << 16), idesc1 = idesc_bf16(M, N, a_mn) | (1u << 16);
+    const uint32_t a_row = (uint32_t)(2 * M / 8) * 128, b_row = (uint32_t)(2 * N / 8) * 128;
+    const uint32_t k_row = (uint32_t)(2 * K / 8) * 128;
+    const uint64_t da = a_mn ? smem_desc(smem_u32(a), a_row, 128) : smem_desc(smem_u32(a), 128, k_row);
+    const uint64_t db = smem_desc(smem_u32(b), b_row, 128);
+    const uint64_t a_step = (a_mn ? 2 * a_row : 256) / 16, b_step = 2 * b_row / 16;  // 16 along K
+    const uint64_t a_lo = (uint64_t)((a_mn ? M : K) / 8) * 128 / 16;
+    bool acc = accumulate;
+    for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t ka = da + ks * a_step, kb = db + ks * b_step;
+        mma_bf16(d_tmem, ka, kb, idesc2, acc);          // hi * [hi | lo]
+        mma_bf16(d_tmem, ka + a_lo, kb, idesc1, true);  // lo * hi
+        acc = true;
+    }
+}
+
 // Both operands K-major: D (+)= A B^T with A [M][2K], B [N][2K].
 __device__ __forceinline__ void mma_split_kk(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
                                              int N, int K, bool accumulate) {
