@@ -677,7 +677,8 @@ __device__ __forceinline__ void tmem_pair(uint32_t taddr, float (&v)[kNS]) {
 //   round B   MMA  K~_c^T U -> tS;  [P_c; P_c] U accumulated onto tA[b], so rows
 //             64-127 become O = Q~ S0 + P U (rows 0-63 are spent)
 //             all: S0 <- gamma_last S0 + tS -> S0 image
-// Copies run ahead: W/Q~ double-buffered two chunks ahead (free once round A of
+// Copies run ahead (issued by one thread of the output warps, so that the MMA
+// issuer never waits on them): W/Q~ double-buffered two chunks ahead (free once round A of
 // the chunk before has completed), K~ once K~^T U has completed, u once the U
 // rows have been read, and P (twice, for the stacked operand) once P U has.
 template <typename T>
@@ -752,7 +753,9 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     const uint32_t tS = tmem, tA0 = tmem + 64;      // tA[b] = tA0 + 64 b
     const uint32_t wl = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes = accumulator rows 32 warp ..
 
-    // thread 0's count of copies and MMA commits issued per barrier (for a clean exit on abort)
+    // Thread 0 issues the MMAs, thread kCopier the bulk copies; each counts what it
+    // issued per barrier (for a clean exit on abort).
+    constexpr int kCopier = 64;
     int wq_iss[2] = {0, 0}, u_iss = 0, k_iss = 0, p_iss = 0, a_iss = 0, b_iss = 0;
     auto rec = [&](int c) { return (size_t)(chunk0 + c) * g.Hv + h; };
     auto load_wq = [&](int c) {
@@ -795,7 +798,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         }
     };
 
-    if (tid == 0) {
+    if (tid == kCopier) {
         load_wq(0);
         if (nch > 1) load_wq(1);
         load_u(0);
@@ -811,13 +814,12 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             umma::mma_split_bpair(tA0 + 64 * b, wqb + b * kWQBytes, false, s0t, 2 * kC, kNS, kDK, false);
             umma::commit(&s_a);
             ++a_iss;
-            if (c > 0) {  // P U of chunk c-1 has completed: the P buffer is free
-                if (!mbar_wait_bounded(&s_o, (uint32_t)((c - 1) & 1))) s_abort = 1;
-                load_p(c);
-            }
         }
         if (warp >= 2) {
-            if (c > 0) out_rows(c - 1);
+            if (c > 0) {
+                out_rows(c - 1);
+                if (tid == kCopier) load_p(c);  // P U of chunk c-1 has completed: the P buffer is free
+            }
         } else {  // U = u - X, rows 0-63
             wait_all(&s_a, (uint32_t)(c & 1));
             wait_all(&s_u, (uint32_t)(c & 1));
@@ -844,8 +846,8 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         umma::fence_after_sync();
 
         // ---- round B: K~^T U and [P; P] U ----
+        if (tid == kCopier && c + 1 < nch) load_u(c + 1);  // the u rows of chunk c have been read (the barrier above)
         if (tid == 0) {
-            if (c + 1 < nch) load_u(c + 1);  // the u rows of chunk c have been read (the barrier above)
             if (!mbar_wait_bounded(&s_k, (uint32_t)(c & 1))) s_abort = 1;
             umma::mma_split_bpair(tS, kt, true, ut, kDK, kNS, kC, false);
             umma::commit(&s_s);
@@ -862,7 +864,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         for (int j = 0; j < kNS; ++j) S[j] = fmaf(glc, S[j], ss[j]);
 #pragma unroll
         for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
-        if (tid == 0) {
+        if (tid == kCopier) {
             if (c + 2 < nch) load_wq(c + 2);  // round A of chunk c has completed: its W/Q~ buffer is free
             if (c + 1 < nch) load_k(c + 1);   // and K~^T U: the K~ buffer is free
         }
@@ -873,15 +875,18 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         umma::fence_after_sync();
     }
     if (!s_abort && warp >= 2) out_rows(nch - 1);
-    if (s_abort && tid == 0) {
-        flag_device_error(&g_chunk_error, 7);
-        // let copies and MMAs still in flight land before TMEM and shared memory are released:
-        // wait for the last issued phase of each barrier (a completed phase returns at once)
+    // on abort, let copies and MMAs still in flight land before TMEM and shared memory
+    // are released: wait for the last issued phase of each barrier (a completed phase
+    // returns at once)
+    if (s_abort && tid == kCopier) {
         for (int b = 0; b < 2; ++b)
             if (wq_iss[b]) mbar_wait_bounded(&s_wq[b], (uint32_t)((wq_iss[b] - 1) & 1));
         if (u_iss) mbar_wait_bounded(&s_u, (uint32_t)((u_iss - 1) & 1));
         if (k_iss) mbar_wait_bounded(&s_k, (uint32_t)((k_iss - 1) & 1));
         if (p_iss) mbar_wait_bounded(&s_p, (uint32_t)((p_iss - 1) & 1));
+    }
+    if (s_abort && tid == 0) {
+        flag_device_error(&g_chunk_error, 7);
         if (a_iss) mbar_wait_bounded(&s_a, (uint32_t)((a_iss - 1) & 1));
         if (b_iss) {
             mbar_wait_bounded(&s_s, (uint32_t)((b_iss - 1) & 1));
