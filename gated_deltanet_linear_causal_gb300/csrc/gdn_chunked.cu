@@ -47,7 +47,8 @@ constexpr int kMaxDV = 128;  // widest head_v_dim handled here
 constexpr int kKC = 4;      // widest conv handled here
 constexpr int kMaxF = 16;   // value heads per key head
 constexpr int kPT = 512;    // chunk-prep threads
-constexpr int kCT = 128;    // chain threads
+constexpr int kCT = 160;    // chain threads: 4 epilogue warps (one state row each) + the MMA issuer's warp
+constexpr int kIssuer = 128;  // the chain thread that issues the MMAs
 constexpr uint32_t kImgBytes = kC * 2 * kDK * 2;  // split [64 tokens][2*128] image: 32 KB
 constexpr uint32_t kPBytes = kC * 2 * kC * 2;     // split [64][2*64] image: 16 KB
 constexpr uint32_t kWQBytes = 2 * kImgBytes;      // W and Q~ of a (chunk, value head)
@@ -670,7 +671,9 @@ __device__ __forceinline__ void tmem_pair(uint32_t taddr, float (&v)[kNS]) {
 }
 
 // Per chunk c (b = c & 1), with M = 128 products (a tcgen05 MMA costs the same
-// issue time at M = 64 and M = 128, so operands are stacked):
+// issue time at M = 64 and M = 128, so operands are stacked).  Warps 0-3 own the
+// 128 state rows; the MMAs are issued by one thread of a fifth warp that takes no
+// part in the epilogues, so issuing round B never delays the state update:
 //   round A   MMA  [W_c; Q~_c] S0 -> tA[b]: rows 0-63 X = W S0, rows 64-127 Q~ S0
 //             (meanwhile warps 2-3 read O of chunk c-1 out of tA[b^1])
 //             warps 0-1: U = u_c - X -> U image
@@ -723,13 +726,15 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     // state rows: thread i holds row i (key dim) of the 32-column slice
     float* Sg = a.ssm_state + ((size_t)(n * g.Hv + h) * kDK + tid) * g.dv + col0;
     float S[kNS];
+    const bool srow = tid < kDK;  // warps 0-3 hold the state rows
 #pragma unroll
     for (int j = 0; j < kNS; j += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(Sg + j);
+        const float4 v = srow ? *reinterpret_cast<const float4*>(Sg + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
     }
+    if (srow)
 #pragma unroll
-    for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
+        for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
 
     if (warp == 0) umma::tmem_alloc(&s_tmem, 256);
     if (tid == 0) {
@@ -753,7 +758,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     const uint32_t tS = tmem, tA0 = tmem + 64;      // tA[b] = tA0 + 64 b
     const uint32_t wl = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes = accumulator rows 32 warp ..
 
-    // Thread 0 issues the MMAs, thread kCopier the bulk copies; each counts what it
+    // Thread kIssuer issues the MMAs, thread kCopier the bulk copies; each counts what it
     // issued per barrier (for a clean exit on abort).
     constexpr int kCopier = 64;
     int wq_iss[2] = {0, 0}, u_iss = 0, k_iss = 0, p_iss = 0, a_iss = 0, b_iss = 0;
@@ -810,17 +815,17 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         const float glc = ws.gl[rec(c)];
         // ---- round A: [W; Q~] S0 ----
         wait_all(&s_wq[b], (uint32_t)((c >> 1) & 1));
-        if (tid == 0) {
+        if (tid == kIssuer) {
             umma::mma_split_bpair(tA0 + 64 * b, wqb + b * kWQBytes, false, s0t, 2 * kC, kNS, kDK, false);
             umma::commit(&s_a);
             ++a_iss;
         }
-        if (warp >= 2) {
+        if (warp == 2 || warp == 3) {
             if (c > 0) {
                 out_rows(c - 1);
                 if (tid == kCopier) load_p(c);  // P U of chunk c-1 has completed: the P buffer is free
             }
-        } else {  // U = u - X, rows 0-63
+        } else if (warp < 2) {  // U = u - X, rows 0-63
             wait_all(&s_a, (uint32_t)(c & 1));
             wait_all(&s_u, (uint32_t)(c & 1));
             umma::fence_after_sync();
@@ -847,7 +852,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
 
         // ---- round B: K~^T U and [P; P] U ----
         if (tid == kCopier && c + 1 < nch) load_u(c + 1);  // the u rows of chunk c have been read (the barrier above)
-        if (tid == 0) {
+        if (tid == kIssuer) {
             if (!mbar_wait_bounded(&s_k, (uint32_t)(c & 1))) s_abort = 1;
             umma::mma_split_bpair(tS, kt, true, ut, kDK, kNS, kC, false);
             umma::commit(&s_s);
@@ -856,14 +861,16 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             umma::commit(&s_o);
             ++b_iss;
         }
-        wait_all(&s_s, (uint32_t)(c & 1));
-        umma::fence_after_sync();
-        float ss[kNS];
-        tmem_pair(tS + wl, ss);
+        if (srow) {
+            wait_all(&s_s, (uint32_t)(c & 1));
+            umma::fence_after_sync();
+            float ss[kNS];
+            tmem_pair(tS + wl, ss);
 #pragma unroll
-        for (int j = 0; j < kNS; ++j) S[j] = fmaf(glc, S[j], ss[j]);
+            for (int j = 0; j < kNS; ++j) S[j] = fmaf(glc, S[j], ss[j]);
 #pragma unroll
-        for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
+            for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
+        }
         if (tid == kCopier) {
             if (c + 2 < nch) load_wq(c + 2);  // round A of chunk c has completed: its W/Q~ buffer is free
             if (c + 1 < nch) load_k(c + 1);   // and K~^T U: the K~ buffer is free
@@ -874,7 +881,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         if (s_abort) break;
         umma::fence_after_sync();
     }
-    if (!s_abort && warp >= 2) out_rows(nch - 1);
+    if (!s_abort && (warp == 2 || warp == 3)) out_rows(nch - 1);
     // on abort, let copies and MMAs still in flight land before TMEM and shared memory
     // are released: wait for the last issued phase of each barrier (a completed phase
     // returns at once)
@@ -885,7 +892,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         if (k_iss) mbar_wait_bounded(&s_k, (uint32_t)((k_iss - 1) & 1));
         if (p_iss) mbar_wait_bounded(&s_p, (uint32_t)((p_iss - 1) & 1));
     }
-    if (s_abort && tid == 0) {
+    if (s_abort && tid == kIssuer) {
         flag_device_error(&g_chunk_error, 7);
         if (a_iss) mbar_wait_bounded(&s_a, (uint32_t)((a_iss - 1) & 1));
         if (b_iss) {
@@ -896,7 +903,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
-    if (s_abort) return;
+    if (s_abort || !srow) return;
 #pragma unroll
     for (int j = 0; j < kNS; j += 4) *reinterpret_cast<float4*>(Sg + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
 }
