@@ -139,6 +139,9 @@ struct PrepSmem {
 // ---- chunk prep ----------------------------------------------------------------
 // Workspace records per (chunk, value head): wq = [W image | Q~ image],
 // kp = [K~ image | P image], u = dv/32 slices of fp32 [64][32], gl = gamma_last.
+// In a u row the 16-byte piece of columns 4k..4k+3 sits at piece k ^ (row & 7), so
+// that the chain's threads, one row each, read their rows without bank conflicts.
+__host__ __device__ constexpr int u_piece(int row, int k) { return k ^ (row & 7); }
 struct ChunkOut {
     unsigned char* wq;
     unsigned char* kp;
@@ -640,7 +643,7 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                 if (lane < 16)
 #pragma unroll
                     for (int q = 0; q < 32; q += 4)
-                        *reinterpret_cast<float4*>(udst + ((size_t)sl * kC + row) * kNS + q) =
+                        *reinterpret_cast<float4*>(udst + ((size_t)sl * kC + row) * kNS + 4 * u_piece(row, q / 4)) =
                             make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
             }
         }
@@ -835,7 +838,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             float uu[kNS];
 #pragma unroll
             for (int j = 0; j < kNS; j += 4) {
-                const float4 u4 = *reinterpret_cast<const float4*>(ur + j);
+                const float4 u4 = *reinterpret_cast<const float4*>(ur + 4 * u_piece(tid, j / 4));
                 uu[j] = __fsub_rn(u4.x, xv[j]);
                 uu[j + 1] = __fsub_rn(u4.y, xv[j + 1]);
                 uu[j + 2] = __fsub_rn(u4.z, xv[j + 2]);
