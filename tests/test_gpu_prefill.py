@@ -242,3 +242,58 @@ def test_prefill_chunked_requires_l2norm():
     with pytest.raises(gb.GdnError) as e:
         _prefill_dev(cfg, x, dev, gb.GDN_PREFILL_CHUNKED, "bf16")
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("K,misaligned", [(1, False), (2, False), (3, False), (4, True), (3, True)])
+def test_prefill_chunked_conv_widths(K, misaligned):
+    """The chunked form's staged conv: widths below 4 (weight rows of K taps) and a
+    conv-weight buffer that starts off a 16-byte boundary (weights then load without the
+    16-byte copies), against the oracle."""
+    dev = device()
+    shape = synth.Shape(2, 4, 128, 64, K)
+    cfg, ocfg = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=140 + K + 7 * misaligned, shape=shape, lengths=[70, 2, 1, 129])
+    cu = x["cu_seqlens"]
+    N, T = len(cu) - 1, int(cu[-1])
+    w = to_dev(x["conv_weight"], dev)
+    if misaligned:
+        buf = torch.empty(w.numel() + 1, dtype=w.dtype, device=dev)
+        buf[1:].copy_(w.reshape(-1))
+        w = buf[1:].view(w.shape)
+        assert w.data_ptr() % 16 != 0
+    d = dict(qkv=to_dev(x["qkv"], dev), gate=to_dev(x["gate"], dev), beta=to_dev(x["beta"], dev),
+             conv=to_dev(x["conv_state"], dev), S=to_dev(x["ssm_state"], dev),
+             out=torch.full((T, shape.num_v_heads, shape.head_v_dim), float("nan"), device=dev))
+    var = gb.GDN_PREFILL_CHUNKED
+    ws = torch.empty(max(1, gb.gdn_prefill_workspace_size(cfg, N, T, var)), dtype=torch.uint8, device=dev)
+    gb.gdn_forward_prefill(cfg, N, to_dev(cu, dev), torch.from_numpy(cu), d["qkv"], w, d["gate"], d["beta"], d["conv"],
+                           d["S"], d["out"], var, ws)
+    o_r, c_r, S_r = _oracle_prefill(ocfg, x)
+    torch.cuda.synchronize()
+    assert_parity(f64(d["out"]), o_r, f64(d["S"]), S_r, what=f"chunked K={K}")
+    assert np.array_equal(f64(d["conv"]), c_r)
+
+
+@pytest.mark.parametrize("cut", [64, 37])
+def test_prefill_chunked_split_equals_whole(cut):
+    """Two chunked calls with carried conv and SSM states agree with one call: the second
+    call's first chunk takes its conv window's head from the carried conv state."""
+    dev = device()
+    shape = synth.Shape(2, 4, 128, 64, 4)
+    cfg, _ = configs(shape, "bf16")
+    x = synth.varlen_prefill(seed=57, shape=shape, lengths=[150])
+    var = gb.GDN_PREFILL_CHUNKED
+    whole = _prefill_dev(cfg, x, dev, var, "bf16")
+    a = dict(x, cu_seqlens=np.array([0, cut], np.int32), qkv=np.ascontiguousarray(x["qkv"][:, :cut]),
+             gate=x["gate"][:cut], beta=x["beta"][:cut])
+    da = _prefill_dev(cfg, a, dev, var, "bf16")
+    torch.cuda.synchronize()
+    b = dict(x, cu_seqlens=np.array([0, 150 - cut], np.int32), qkv=np.ascontiguousarray(x["qkv"][:, cut:]),
+             gate=x["gate"][cut:], beta=x["beta"][cut:],
+             conv_state=da["conv"].cpu().view(torch.int16).numpy().view(np.uint16),
+             ssm_state=da["S"].cpu().numpy())
+    db = _prefill_dev(cfg, b, dev, var, "bf16")
+    torch.cuda.synchronize()
+    out = torch.cat([da["out"], db["out"]])
+    assert np.array_equal(bits(db["conv"]), bits(whole["conv"]))
+    assert_parity(f64(out), f64(whole["out"]), f64(db["S"]), f64(whole["S"]), what="chunked split vs whole")
