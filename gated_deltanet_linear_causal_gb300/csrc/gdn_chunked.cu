@@ -10,7 +10,8 @@
 //   S_end = gamma_last S0 + K~^T U,  K~ = diag(c) K,
 // where row t of U is the token's delta (beta_t (v_t - v_pred)).  Only the
 // products with S0 depend on the previous chunk, so:
-//   chunk_prep_kernel  (every chunk x key head in parallel) runs steps 1-4 on
+//   chunk_prep_kernel  (every chunk x key head in parallel, persistent CTAs that
+//       start the next item's raw copies early) runs steps 1-4 on
 //       the chunk's raw qkv columns (the conv window reaching back into the
 //       previous chunk or the carried conv state), forms K K^T and Q K^T on the
 //       tensor cores, then for each value head of the key head T, and W and u
@@ -398,7 +399,7 @@ __device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float
 
 template <typename T>
 __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a, const int32_t* __restrict__ coff,
-                                                            const ChunkOut ws, const GateParams gp) {
+                                                            const ChunkOut ws, const GateParams gp, const int nchunk) {
     using L = PrepSmem<T>;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* kimg = smem + L::kimg;
@@ -421,237 +422,276 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ int s_fail;
 
-    const int chunk = blockIdx.x, hk = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = seq_of_chunk(coff, a.N, chunk);
-    const int tb = a.cu[n];
-    const int t0 = tb + (chunk - coff[n]) * kC;
-    const int cnt = min(kC, a.cu[n + 1] - t0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = g.K;
-    const bool first = t0 - (K - 1) < tb;  // the conv window reaches into the carried conv state
     constexpr int kBarV = 1, kBarT = 2, kGrp = kPT / 2;  // warps 8-15: V; warps 0-7: A, T
-    const int cbq = hk * kDK, cbk = (g.Hk + hk) * kDK;
-    auto cbv = [&](int j) { return 2 * g.Hk * kDK + (hk * f + j) * g.dv; };
-    // raw inputs of Q (and, with two buffers, of K) start copying at once
-    issue_raw<T>(a, rbuf(0), cbq, kDK, tb, t0, tid, kPT);
-    if (R::bufs == 2) issue_raw<T>(a, rbuf(1), cbk, kDK, tb, t0, tid, kPT);
+    // Persistent: CTA b takes items b, b + gridDim.x, ... of the (key head, chunk) items,
+    // chunks fastest.  With two raw buffers the value-head warps start the next item's Q
+    // and K copies as soon as their last convolutions free the buffers.
+    const int nitems = nchunk * g.Hk;
+    struct Item {
+        int chunk, hk, n, tb, t0, cnt;
+        bool first;  // the conv window reaches into the carried conv state
+    };
+    auto item_at = [&](int it) {
+        Item x;
+        x.chunk = it % nchunk;
+        x.hk = it / nchunk;
+        x.n = seq_of_chunk(coff, a.N, x.chunk);
+        x.tb = a.cu[x.n];
+        x.t0 = x.tb + (x.chunk - coff[x.n]) * kC;
+        x.cnt = min(kC, a.cu[x.n + 1] - x.t0);
+        x.first = x.t0 - (K - 1) < x.tb;
+        return x;
+    };
+    auto cbq = [&](const Item& x) { return x.hk * kDK; };
+    auto cbk = [&](const Item& x) { return (g.Hk + x.hk) * kDK; };
+    int item = blockIdx.x;
+    if (item >= nitems) return;
+    Item cur = item_at(item);
+    if (R::bufs == 2) {  // the first item's raw Q and K start copying at once
+        issue_raw<T>(a, rbuf(0), cbq(cur), kDK, cur.tb, cur.t0, tid, kPT);
+        issue_raw<T>(a, rbuf(1), cbk(cur), kDK, cur.tb, cur.t0, tid, kPT);
+    }
     if (warp == 0) umma::tmem_alloc(&s_tmem, 512);
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         fence_mbar_init();
         s_fail = 0;
     }
-    // log-decays and betas of the value heads
-    for (int idx = tid; idx < f * kC; idx += kPT) {
-        const int j = idx / kC, t = idx - j * kC;
-        const bool in = t < cnt;
-        sG[idx] = in ? gate_of(gp.A_log, gp.dt_bias, a.gate[(size_t)(t0 + t) * g.Hv + hk * f + j], hk * f + j) : 0.f;
-        sBet[idx] = in ? beta_of(gp.A_log, a.beta[(size_t)(t0 + t) * g.Hv + hk * f + j]) : 0.f;
-    }
-
-    // ---- steps 1-4 for Q, then K: conv + SiLU, L2 norm (1/sqrt(dk) for Q) ----
-    // thread (t, part): token t = tid % 64, channels 16*part .. +15 of the head;
-    // lanes run along tokens, so operand-image rows are written 16 bytes apart
-    for (int pass = 0; pass < 2; ++pass) {
-        const int cb = pass == 0 ? cbq : cbk;
-        const RawBuf<T> rb = rbuf(R::bufs == 2 ? pass : 0);
-        if (R::bufs == 1 && pass == 1) issue_raw<T>(a, rb, cbk, kDK, tb, t0, tid, kPT);
-        // pending groups newer than this pass's: K during pass 0, and V0 (value-head
-        // warps) during pass 1, with two buffers
-        if (R::bufs == 2 && (pass == 0 || tid >= kGrp)) cp_async_wait<1>();
-        else cp_async_wait<0>();
-        __syncthreads();
-        if (first) {
-            fill_conv_state<T>(a, rb, cb, kDK, n, tb, t0, tid, kPT);
-            __syncthreads();
-        }
-        if (pass == 0) {
-            scan_heads(sG, f);
-            for (int idx = tid; idx < f * kC; idx += kPT) {
-                const int j = idx / kC;
-                const float G = sG[idx];
-                sGam[idx] = expf(G);
-                sCd[idx] = expf(sG[j * kC + kC - 1] - G);
-            }
-            if (tid < f) ws.gl[(size_t)chunk * g.Hv + hk * f + tid] = expf(sG[tid * kC + kC - 1]);
-        }
-        const int t = tid & (kC - 1), part = tid >> 6;
-        float v[16];
-        float ss = 0.f;
-#pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-            float y[8];
-            conv8(rb, t, 16 * part + 8 * gi, K, y);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                v[8 * gi + e] = y[e];
-                ss = fmaf(y[e], y[e], ss);
-            }
-        }
-        nrm[part * kC + t] = ss;
-        __syncthreads();
-        float tot = 0.f;
-#pragma unroll
-        for (int p = 0; p < 8; ++p) tot += nrm[p * kC + t];
-        const float r = g.use_l2 ? rsqrtf(tot + g.eps) : 1.f;
-        const float fac = pass ? r : __fmul_rn(g.q_scale, r);
-        const bool in = t < cnt;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = in ? __fmul_rn(v[e], fac) : 0.f;
-        unsigned char* img = pass ? kimg : qimg;
-        umma::store_split8(img, t, 16 * part, kDK, v);
-        umma::store_split8(img, t, 16 * part + 8, kDK, v + 8);
-        for (int j = 0; j < f; ++j) {  // Q~ = diag(gamma) Q and K~ = diag(c) K of each value head
-            const size_t rec = (size_t)chunk * g.Hv + hk * f + j;
-            const float sc = pass ? sCd[j * kC + t] : sGam[j * kC + t];
-            unsigned char* dst = pass ? ws.kp + rec * kKPBytes : ws.wq + rec * kWQBytes + kImgBytes;
-            float sv[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sv[e] = __fmul_rn(sc, v[e]);
-            umma::store_split8(dst, t, 16 * part, kDK, sv);
-            umma::store_split8(dst, t, 16 * part + 8, kDK, sv + 8);
-        }
-        __syncthreads();  // the partial sums are reused by the next pass; the raw buffer is free
-        // with two buffers, value head `pass` starts copying into the buffer just freed
-        if (R::bufs == 2 && tid >= kGrp && pass < f) issue_raw<T>(a, rb, cbv(pass), g.dv, tb, t0, tid - kGrp, kGrp);
-    }
-
-    // ---- [K; Q] K^T on the tensor cores: rows 0-63 K K^T, rows 64-127 Q K^T ----
-    fence_proxy_async_smem();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = s_tmem;
-    const uint32_t tG = tmem, tW = tmem + 128, tU = tmem + 256;
-    if (tid == 0) {
-        umma::mma_split(tG, kimg, false, kimg, false, 2 * kC, kC, kDK, false);
-        umma::commit(&s_bar);
-    }
     uint32_t phase = 0;
-    const uint32_t wl = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
-    const int row = 16 * (warp & 3) + (lane & 15);          // M = 64 rows sit in lanes 0-15 of each quarter
-    for (int j = 0; j < f; ++j) {
-        const int h = hk * f + j;
-        const size_t rec = (size_t)chunk * g.Hv + h;
-        if (warp < 8) {
-            const float* Gj = sG + j * kC;
-            const float* Bj = sBet + j * kC;
-            const float* Yj = sGam + j * kC;
-            if (j == 0) {  // the Gram matrices into shared memory
-                if (!mbar_wait_bounded(&s_bar, 0)) s_fail = 1;
-                umma::fence_after_sync();
-                const int lr = 32 * (warp & 3) + lane;  // M = 128: row = TMEM lane
-                float v[32];
-                umma::tmem_ld32(tG + wl + 32 * (warp >> 2), v);
-                float* dst = lr < kC ? kk + lr * kLd : qk + (lr - kC) * kLd;
-#pragma unroll
-                for (int q = 0; q < 32; ++q) dst[32 * (warp >> 2) + q] = v[q];
-                named_sync(kBarT, kGrp);
-            }
-            // A (strictly lower) and P; lanes along t
-            unsigned char* pimg = ws.kp + rec * kKPBytes + kImgBytes;
-            for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
-                const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
-                float pv[8], av[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = s0 + e;
-                    const float dec = s <= t ? expf(Gj[t] - Gj[s]) : 0.f;
-                    av[e] = s < t ? __fmul_rn(__fmul_rn(Bj[t], dec), kk[t * kLd + s]) : 0.f;
-                    pv[e] = __fmul_rn(dec, qk[t * kLd + s]);
-                }
-                *reinterpret_cast<float4*>(Ab + t * kAld + s0) = make_float4(av[0], av[1], av[2], av[3]);
-                *reinterpret_cast<float4*>(Ab + t * kAld + s0 + 4) = make_float4(av[4], av[5], av[6], av[7]);
-                umma::store_split8(pimg, t, s0, kC, pv);
-            }
-            named_sync(kBarT, kGrp);
-            inverse_blocked(Ab, Tb, reinterpret_cast<float*>(timg), tid, kBarT);
-            // T diag(beta gamma) and T diag(beta) as A operands
-            for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
-                const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
-                const float4 tl = ld4(Tb + t * kAld + s0), th = ld4(Tb + t * kAld + s0 + 4);
-                const float trow[8] = {tl.x, tl.y, tl.z, tl.w, th.x, th.y, th.z, th.w};
-                float tg[8], tbt[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int s = s0 + e;
-                    const float tv = trow[e];
-                    tg[e] = __fmul_rn(tv, __fmul_rn(Bj[s], Yj[s]));
-                    tbt[e] = __fmul_rn(tv, Bj[s]);
-                }
-                umma::store_split8(timg, t, s0, kC, tg);
-                umma::store_split8(timg + kPBytes, t, s0, kC, tbt);
-            }
-        } else {
-            // ---- V: conv + SiLU of the head's raw inputs into the V image ----
-            const int vt = tid - kGrp;
-            const RawBuf<T> rb = rbuf(R::bufs == 2 ? (j & 1) : 0);
-            if (R::bufs == 1) issue_raw<T>(a, rb, cbv(j), g.dv, tb, t0, vt, kGrp);
-            if (R::bufs == 2 && j + 1 < f) cp_async_wait<1>();  // value head j+1 may still be copying
-            else cp_async_wait<0>();
-            if (j == 0 && !mbar_wait_bounded(&s_bar, 0)) s_fail = 1;  // the Q image is free once the Gram products are done
-            named_sync(kBarV, kGrp);
-            if (first) {
-                fill_conv_state<T>(a, rb, cbv(j), g.dv, n, tb, t0, vt, kGrp);
-                named_sync(kBarV, kGrp);
-            }
-            for (int idx = vt; idx < (kC / 2) * (g.dv / 8); idx += kGrp) {  // lanes along token pairs
-                const int t = 2 * (idx & (kC / 2 - 1)), c = 8 * (idx >> 5);
-                float y0[8], y1[8];
-                conv8x2(rb, t, c, K, y0, y1);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (t >= cnt) y0[e] = 0.f;
-                    if (t + 1 >= cnt) y1[e] = 0.f;
-                }
-                umma::store_split8(qimg, t, c, g.dv, y0);
-                umma::store_split8(qimg, t + 1, c, g.dv, y1);
-            }
-            if (R::bufs == 2 && j + 2 < f) {  // the buffer is free: value head j+2 starts copying
-                named_sync(kBarV, kGrp);
-                issue_raw<T>(a, rb, cbv(j + 2), g.dv, tb, t0, vt, kGrp);
-            }
+    bool prefetched = false;  // cur's raw Q and K were started during the previous item
+    for (;;) {
+        const int chunk = cur.chunk, hk = cur.hk, n = cur.n, tb = cur.tb, t0 = cur.t0, cnt = cur.cnt;
+        const bool first = cur.first;
+        auto cbv = [&](int j) { return 2 * g.Hk * kDK + (hk * f + j) * g.dv; };
+        const int next_item = item + (int)gridDim.x;
+        const bool has_next = next_item < nitems;
+        const Item nx = has_next ? item_at(next_item) : cur;
+        // log-decays and betas of the value heads
+        for (int idx = tid; idx < f * kC; idx += kPT) {
+            const int j = idx / kC, t = idx - j * kC;
+            const bool in = t < cnt;
+            sG[idx] = in ? gate_of(gp.A_log, gp.dt_bias, a.gate[(size_t)(t0 + t) * g.Hv + hk * f + j], hk * f + j) : 0.f;
+            sBet[idx] = in ? beta_of(gp.A_log, a.beta[(size_t)(t0 + t) * g.Hv + hk * f + j]) : 0.f;
         }
-        if (j == 0 && !s_fail) phase ^= 1;
+
+        // ---- steps 1-4 for Q, then K: conv + SiLU, L2 norm (1/sqrt(dk) for Q) ----
+        // thread (t, part): token t = tid % 64, channels 16*part .. +15 of the head;
+        // lanes run along tokens, so operand-image rows are written 16 bytes apart
+        for (int pass = 0; pass < 2; ++pass) {
+            const int cb = pass == 0 ? cbq(cur) : cbk(cur);
+            const RawBuf<T> rb = rbuf(R::bufs == 2 ? pass : 0);
+            if (R::bufs == 1) issue_raw<T>(a, rb, cb, kDK, tb, t0, tid, kPT);
+            // with two buffers, pending groups newer than this pass's: K during pass 0 (unless
+            // Q and K were started during the previous item, in either order), and V0
+            // (value-head warps) during pass 1
+            if (R::bufs == 2 && ((pass == 0 && !prefetched) || (pass == 1 && tid >= kGrp))) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            __syncthreads();
+            if (first) {
+                fill_conv_state<T>(a, rb, cb, kDK, n, tb, t0, tid, kPT);
+                __syncthreads();
+            }
+            if (pass == 0) {
+                scan_heads(sG, f);
+                for (int idx = tid; idx < f * kC; idx += kPT) {
+                    const int j = idx / kC;
+                    const float G = sG[idx];
+                    sGam[idx] = expf(G);
+                    sCd[idx] = expf(sG[j * kC + kC - 1] - G);
+                }
+                if (tid < f) ws.gl[(size_t)chunk * g.Hv + hk * f + tid] = expf(sG[tid * kC + kC - 1]);
+            }
+            const int t = tid & (kC - 1), part = tid >> 6;
+            float v[16];
+            float ss = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+                float y[8];
+                conv8(rb, t, 16 * part + 8 * gi, K, y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    v[8 * gi + e] = y[e];
+                    ss = fmaf(y[e], y[e], ss);
+                }
+            }
+            nrm[part * kC + t] = ss;
+            __syncthreads();
+            float tot = 0.f;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) tot += nrm[p * kC + t];
+            const float r = g.use_l2 ? rsqrtf(tot + g.eps) : 1.f;
+            const float fac = pass ? r : __fmul_rn(g.q_scale, r);
+            const bool in = t < cnt;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = in ? __fmul_rn(v[e], fac) : 0.f;
+            unsigned char* img = pass ? kimg : qimg;
+            umma::store_split8(img, t, 16 * part, kDK, v);
+            umma::store_split8(img, t, 16 * part + 8, kDK, v + 8);
+            for (int j = 0; j < f; ++j) {  // Q~ = diag(gamma) Q and K~ = diag(c) K of each value head
+                const size_t rec = (size_t)chunk * g.Hv + hk * f + j;
+                const float sc = pass ? sCd[j * kC + t] : sGam[j * kC + t];
+                unsigned char* dst = pass ? ws.kp + rec * kKPBytes : ws.wq + rec * kWQBytes + kImgBytes;
+                float sv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sv[e] = __fmul_rn(sc, v[e]);
+                umma::store_split8(dst, t, 16 * part, kDK, sv);
+                umma::store_split8(dst, t, 16 * part + 8, kDK, sv + 8);
+            }
+            __syncthreads();  // the partial sums are reused by the next pass; the raw buffer is free
+            // with two buffers, value head `pass` starts copying into the buffer just freed
+            if (R::bufs == 2 && tid >= kGrp && pass < f) issue_raw<T>(a, rb, cbv(pass), g.dv, tb, t0, tid - kGrp, kGrp);
+        }
+
+        // ---- [K; Q] K^T on the tensor cores: rows 0-63 K K^T, rows 64-127 Q K^T ----
         fence_proxy_async_smem();
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
-        if (s_fail) break;
+        const uint32_t tmem = s_tmem;
+        const uint32_t tG = tmem, tW = tmem + 128, tU = tmem + 256;
         if (tid == 0) {
-            umma::mma_split(tW, timg, false, kimg, true, kC, kDK, kC, false);             // W = T diag(beta gamma) K
-            umma::mma_split(tU, timg + kPBytes, false, qimg, true, kC, g.dv, kC, false);  // u = T diag(beta) V
+            umma::mma_split(tG, kimg, false, kimg, false, 2 * kC, kC, kDK, false);
             umma::commit(&s_bar);
         }
-        const bool done = mbar_wait_bounded(&s_bar, phase);
-        if (!done) s_fail = 1;
-        umma::fence_after_sync();
-        const int cq = warp >> 3;  // column half
-        if ((warp & 4) == 0) {     // warps 0-3, 8-11: W rows as a split operand image, 64 columns each
-            unsigned char* wdst = ws.wq + rec * kWQBytes;
-            for (int c0 = 64 * cq; c0 < 64 * cq + 64; c0 += 32) {
-                float v[32];
-                umma::tmem_ld32(tW + wl + c0, v);
-                if (lane < 16)
+        const uint32_t wl = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
+        const int row = 16 * (warp & 3) + (lane & 15);          // M = 64 rows sit in lanes 0-15 of each quarter
+        for (int j = 0; j < f; ++j) {
+            const int h = hk * f + j;
+            const size_t rec = (size_t)chunk * g.Hv + h;
+            if (warp < 8) {
+                const float* Gj = sG + j * kC;
+                const float* Bj = sBet + j * kC;
+                const float* Yj = sGam + j * kC;
+                if (j == 0) {  // the Gram matrices into shared memory
+                    if (!mbar_wait_bounded(&s_bar, phase)) s_fail = 1;
+                    umma::fence_after_sync();
+                    const int lr = 32 * (warp & 3) + lane;  // M = 128: row = TMEM lane
+                    float v[32];
+                    umma::tmem_ld32(tG + wl + 32 * (warp >> 2), v);
+                    float* dst = lr < kC ? kk + lr * kLd : qk + (lr - kC) * kLd;
 #pragma unroll
-                    for (int q = 0; q < 32; q += 8) umma::store_split8(wdst, row, c0 + q, kDK, v + q);
-            }
-        } else {  // warps 4-7, 12-15: u rows, fp32, one [64][32] block per 32-column slice
-            float* udst = ws.u + rec * kC * g.dv;
-            for (int sl = 2 * cq; sl < 2 * cq + 2 && sl < g.dv / kNS; ++sl) {
-                float v[32];
-                umma::tmem_ld32(tU + wl + kNS * sl, v);
-                if (lane < 16)
+                    for (int q = 0; q < 32; ++q) dst[32 * (warp >> 2) + q] = v[q];
+                    named_sync(kBarT, kGrp);
+                }
+                // A (strictly lower) and P; lanes along t
+                unsigned char* pimg = ws.kp + rec * kKPBytes + kImgBytes;
+                for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
+                    const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
+                    float pv[8], av[8];
 #pragma unroll
-                    for (int q = 0; q < 32; q += 4)
-                        *reinterpret_cast<float4*>(udst + ((size_t)sl * kC + row) * kNS + 4 * u_piece(row, q / 4)) =
-                            make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = s0 + e;
+                        const float dec = s <= t ? expf(Gj[t] - Gj[s]) : 0.f;
+                        av[e] = s < t ? __fmul_rn(__fmul_rn(Bj[t], dec), kk[t * kLd + s]) : 0.f;
+                        pv[e] = __fmul_rn(dec, qk[t * kLd + s]);
+                    }
+                    *reinterpret_cast<float4*>(Ab + t * kAld + s0) = make_float4(av[0], av[1], av[2], av[3]);
+                    *reinterpret_cast<float4*>(Ab + t * kAld + s0 + 4) = make_float4(av[4], av[5], av[6], av[7]);
+                    umma::store_split8(pimg, t, s0, kC, pv);
+                }
+                named_sync(kBarT, kGrp);
+                inverse_blocked(Ab, Tb, reinterpret_cast<float*>(timg), tid, kBarT);
+                // T diag(beta gamma) and T diag(beta) as A operands
+                for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
+                    const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
+                    const float4 tl = ld4(Tb + t * kAld + s0), th = ld4(Tb + t * kAld + s0 + 4);
+                    const float trow[8] = {tl.x, tl.y, tl.z, tl.w, th.x, th.y, th.z, th.w};
+                    float tg[8], tbt[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = s0 + e;
+                        const float tv = trow[e];
+                        tg[e] = __fmul_rn(tv, __fmul_rn(Bj[s], Yj[s]));
+                        tbt[e] = __fmul_rn(tv, Bj[s]);
+                    }
+                    umma::store_split8(timg, t, s0, kC, tg);
+                    umma::store_split8(timg + kPBytes, t, s0, kC, tbt);
+                }
+            } else {
+                // ---- V: conv + SiLU of the head's raw inputs into the V image ----
+                const int vt = tid - kGrp;
+                const RawBuf<T> rb = rbuf(R::bufs == 2 ? (j & 1) : 0);
+                if (R::bufs == 1) issue_raw<T>(a, rb, cbv(j), g.dv, tb, t0, vt, kGrp);
+                // one newer group may still be copying: value head j+1, or for the last head the
+                // next item's Q or K started after head j-1
+                if (R::bufs == 2 && (j + 1 < f || (j >= 1 && has_next))) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                if (j == 0 && !mbar_wait_bounded(&s_bar, phase)) s_fail = 1;  // the Q image is free once the Gram products are done
+                named_sync(kBarV, kGrp);
+                if (first) {
+                    fill_conv_state<T>(a, rb, cbv(j), g.dv, n, tb, t0, vt, kGrp);
+                    named_sync(kBarV, kGrp);
+                }
+                for (int idx = vt; idx < (kC / 2) * (g.dv / 8); idx += kGrp) {  // lanes along token pairs
+                    const int t = 2 * (idx & (kC / 2 - 1)), c = 8 * (idx >> 5);
+                    float y0[8], y1[8];
+                    conv8x2(rb, t, c, K, y0, y1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (t >= cnt) y0[e] = 0.f;
+                        if (t + 1 >= cnt) y1[e] = 0.f;
+                    }
+                    umma::store_split8(qimg, t, c, g.dv, y0);
+                    umma::store_split8(qimg, t + 1, c, g.dv, y1);
+                }
+                if (R::bufs == 2 && j + 2 < f) {  // the buffer is free: value head j+2 starts copying
+                    named_sync(kBarV, kGrp);
+                    issue_raw<T>(a, rb, cbv(j + 2), g.dv, tb, t0, vt, kGrp);
+                } else if (R::bufs == 2 && has_next) {  // the buffer is free for good: the next item's Q or K
+                    named_sync(kBarV, kGrp);
+                    if ((j & 1) == 0) issue_raw<T>(a, rbuf(0), cbq(nx), kDK, nx.tb, nx.t0, vt, kGrp);
+                    else issue_raw<T>(a, rbuf(1), cbk(nx), kDK, nx.tb, nx.t0, vt, kGrp);
+                    if (f == 1) issue_raw<T>(a, rbuf(1), cbk(nx), kDK, nx.tb, nx.t0, vt, kGrp);  // idle since the K pass
+                }
             }
+            if (j == 0 && !s_fail) phase ^= 1;
+            fence_proxy_async_smem();
+            umma::fence_before_sync();
+            __syncthreads();
+            umma::fence_after_sync();
+            if (s_fail) break;
+            if (tid == 0) {
+                umma::mma_split(tW, timg, false, kimg, true, kC, kDK, kC, false);             // W = T diag(beta gamma) K
+                umma::mma_split(tU, timg + kPBytes, false, qimg, true, kC, g.dv, kC, false);  // u = T diag(beta) V
+                umma::commit(&s_bar);
+            }
+            const bool done = mbar_wait_bounded(&s_bar, phase);
+            if (!done) s_fail = 1;
+            umma::fence_after_sync();
+            const int cq = warp >> 3;  // column half
+            if ((warp & 4) == 0) {     // warps 0-3, 8-11: W rows as a split operand image, 64 columns each
+                unsigned char* wdst = ws.wq + rec * kWQBytes;
+                for (int c0 = 64 * cq; c0 < 64 * cq + 64; c0 += 32) {
+                    float v[32];
+                    umma::tmem_ld32(tW + wl + c0, v);
+                    if (lane < 16)
+#pragma unroll
+                        for (int q = 0; q < 32; q += 8) umma::store_split8(wdst, row, c0 + q, kDK, v + q);
+                }
+            } else {  // warps 4-7, 12-15: u rows, fp32, one [64][32] block per 32-column slice
+                float* udst = ws.u + rec * kC * g.dv;
+                for (int sl = 2 * cq; sl < 2 * cq + 2 && sl < g.dv / kNS; ++sl) {
+                    float v[32];
+                    umma::tmem_ld32(tU + wl + kNS * sl, v);
+                    if (lane < 16)
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4)
+                            *reinterpret_cast<float4*>(udst + ((size_t)sl * kC + row) * kNS + 4 * u_piece(row, q / 4)) =
+                                make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+                }
+            }
+            if (done) phase ^= 1;
+            umma::fence_before_sync();
+            __syncthreads();  // tensor memory, the V image, raw inputs and the T images are free for the next head
+            umma::fence_after_sync();
+            if (s_fail) break;
         }
-        if (done) phase ^= 1;
-        umma::fence_before_sync();
-        __syncthreads();  // tensor memory, the V image, raw inputs and the T images are free for the next head
-        umma::fence_after_sync();
-        if (s_fail) break;
+        if (s_fail || !has_next) break;
+        item = next_item;
+        cur = nx;
+        prefetched = R::bufs == 2;
     }
     if (s_fail && tid == 0) {
         flag_device_error(&g_chunk_error, 7);
@@ -660,7 +700,7 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     cp_async_wait<0>();  // after an early exit, copies issued for later value heads may still be landing
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_free(tmem, 512);
+    if (warp == 0) umma::tmem_free(s_tmem, 512);
 }
 
 // ---- chain ----------------------------------------------------------------------
@@ -962,7 +1002,12 @@ cudaError_t launch_chunked_t(const PrefillArgs& a, const GateParams& gp, int nch
     const size_t prep_smem = PrepSmem<T>::total(g.f);
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
-    chunk_prep_kernel<T><<<dim3(nchunk, g.Hk), kPT, prep_smem, stream>>>(a, coff, out, gp);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int nitems = nchunk * g.Hk;
+    chunk_prep_kernel<T><<<std::min(nitems, sms), kPT, prep_smem, stream>>>(a, coff, out, gp, nchunk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chain_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
