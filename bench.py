@@ -110,6 +110,21 @@ def _dist():
     return None, 0, 1
 
 
+def _max_over_ranks(dist, ms, dev):
+    """The job's time: the slowest rank's (every rank passes its own)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_value(units_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed over the job's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def _to_dev(arr, dev):
     import numpy as np
     import torch
@@ -208,13 +223,8 @@ def run_decode(args, dev, dist, rank, world, st, steps):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = B_DECODE * args.steps * world
-    value = tokens / (ms / 1e3)
+    ms = _max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    value = _job_value(B_DECODE * args.steps, world, ms)
     launch_us = ms * 1e3 / args.steps
 
     if args.no_e2e:
@@ -276,15 +286,12 @@ def run_decode(args, dev, dist, rank, world, st, steps):
             stream.wait_event(ev_out[k])
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = _max_over_ranks(dist, e0.elapsed_time(e1), dev)
     h2d = nbytes
     d2h = h_out[0].numel() * 4
     return dict(ms=ms, value=value, launch_us=launch_us, bytes=per_step, rotation=R,
-                e2e=None if args.no_e2e else dict(value=tokens / (ms_e2e / 1e3), unit="tokens/s", h2d_bytes_per_step=h2d,
+                e2e=None if args.no_e2e else dict(value=_job_value(B_DECODE * args.steps, world, ms_e2e), unit="tokens/s",
+                         h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h, overlap="H2D and D2H streams, two buffer sets: copies of "
                          "neighbouring steps overlap the kernel"), inputs=dict(steps=steps, state=st))
 
