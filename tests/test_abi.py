@@ -121,3 +121,32 @@ def test_binding_rejects_cpu_tensors(lib):
     t = torch.zeros(10)
     with pytest.raises(ValueError):
         binding.gdn_forward_decode(cfg, 1, t, t, t, t, t, t, t)
+
+
+def test_gated_norm_and_gated_decode_validation(lib):
+    cfg = _cfg()
+    F = ctypes.c_float
+    # gdn_gated_rmsnorm(cfg, rows, o, z, weight, eps, y, stream)
+    norm = lambda rows, p=(FAKE,) * 3, eps=1e-6, y=FAKE: lib.gdn_gated_rmsnorm(ctypes.byref(cfg), rows, *p, F(eps), y, None)
+    assert norm(0) == 0                                        # no rows: no-op
+    assert norm(-1) == 2
+    assert norm(4, eps=-1.0) == 2                              # eps must be >= 0 and finite
+    assert norm(4, eps=float("nan")) == 2
+    assert norm(4, p=(0, FAKE, FAKE)) == 1                     # NULL o
+    assert norm(4, p=(FAKE, FAKE + 2, FAKE)) == 3              # z not 16-byte aligned
+    assert norm(4, y=FAKE + 8) == 3
+    # gdn_forward_decode_gated(cfg, B, qkv, w, gate, beta, conv, S, z, norm_w, eps, y, stream)
+    def dg(c, batch=1, ptrs=None, eps=1e-6, y=FAKE):
+        p = ptrs or [FAKE] * 8
+        return lib.gdn_forward_decode_gated(ctypes.byref(c), batch, *p[:6], p[6], p[7], F(eps), y, None)
+    assert dg(_cfg(head_v_dim=64)) == 8                        # the fused norm runs in the d_v = 128 kernel only
+    assert dg(cfg, batch=-1) == 2
+    assert dg(cfg, eps=-1.0) == 2
+    assert dg(cfg, batch=0, ptrs=[0] * 8) == 0                 # batch 0: no-op, pointers unused
+    p = [FAKE] * 8
+    p[6] = 0
+    assert dg(cfg, ptrs=p) == 1                                # NULL z
+    p = [FAKE] * 8
+    p[7] = FAKE + 4
+    assert dg(cfg, ptrs=p) == 3                                # norm weight not 16-byte aligned
+    assert dg(cfg, y=FAKE + 2) == 3
