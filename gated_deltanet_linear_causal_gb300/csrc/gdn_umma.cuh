@@ -29,14 +29,6 @@ __device__ __forceinline__ uint32_t kmajor_offset(int r, int k, int ktot) {
     return (uint32_t)((r >> 3) * (ktot >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
 
-// Store fp32 x at (r, k) of a split operand with K logical columns (ktot = 2K).
-__device__ __forceinline__ void store_split(unsigned char* base, int r, int k, int K, float x) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-    *reinterpret_cast<__nv_bfloat16*>(base + kmajor_offset(r, k, 2 * K)) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(base + kmajor_offset(r, K + k, 2 * K)) = lo;
-}
-
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
@@ -104,12 +96,6 @@ __device__ __forceinline__ void mma_split_bpair(uint32_t d_tmem, const unsigned 
     }
 }
 
-// Both operands K-major: D (+)= A B^T with A [M][2K], B [N][2K].
-__device__ __forceinline__ void mma_split_kk(uint32_t d_tmem, const unsigned char* a, const unsigned char* b, int M,
-                                             int N, int K, bool accumulate) {
-    mma_split(d_tmem, a, false, b, false, M, N, K, accumulate);
-}
-
 // Store 8 consecutive fp32 values as the hi and lo halves of row r, columns
 // c0..c0+7 (c0 % 8 == 0) of a split operand image with N logical columns:
 // two 16-byte stores.
@@ -160,10 +146,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
-
-// TMEM address of row `row` of an accumulator at column `col`: M = 128 puts row r
-// in lane r; M = 64 puts row r in lane (r % 16) + 32 * (r / 16).
-__device__ __forceinline__ uint32_t lane_of(int row, int M) { return M == 128 ? (uint32_t)row : (uint32_t)((row & 15) + 32 * (row >> 4)); }
 
 }  // namespace umma
 }  // namespace gdn
