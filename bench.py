@@ -479,6 +479,29 @@ def _spread(times):
 # fp64 oracle on the host cores
 # ---------------------------------------------------------------------------
 
+def _host_cpu():
+    """The host the oracle runs on: its logical core count and CPU model."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine()}
+
+
 def oracle_decode_rate(steps, state, budget_s, max_steps):
     """Oracle decode steps of the B=64 workload (all sequences, all heads) until the
     time budget is spent; returns (tokens/s, sample description)."""
@@ -603,7 +626,7 @@ def main():
     if world == 1 and args.cpu_budget > 0:
         v, sample = oracle_decode_rate(dec["inputs"]["steps"], dec["inputs"]["state"], args.cpu_budget, args.steps)
         line["cpu_baseline"] = {"value": round(v, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": sample}
+                                "sample": sample, **_host_cpu()}
     if sec:
         line["secondary"] = sec
     print(json.dumps(line), flush=True)
@@ -631,7 +654,7 @@ def main_reference(args):
             "config": {"workload": "decode B=64, H_k=16, H_v=32, d_k=d_v=128, K=4, bf16 qkv (fp64 oracle)",
                        "global_batch": B_DECODE, "seq_len": 1, "parallelism": "host, 1 thread"},
             "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **_host_cpu()},
             "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(total, 2)}
     print(json.dumps(line), flush=True)

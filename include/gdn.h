@@ -134,7 +134,11 @@ size_t gdn_prefill_workspace_size(const gdn_config_t *cfg, int32_t num_seqs,
 /*
  * Prefill of `num_seqs` sequences packed back to back: sequence n is tokens
  * [cu[n], cu[n+1]) and runs exactly as if alone, from its own states; the
- * conv window never crosses a sequence boundary.
+ * conv window never crosses a sequence boundary.  (MNN "Qwen3.5" page: section
+ * 1.2 gives the layer over qkv [B, D, L] with all five steps per token, and
+ * section 1.4 the per-sequence conv state [B, D, K-1] and recurrent state
+ * [B, H, d_k, d_v] that carry across calls; the pages state no packing, so a
+ * packed sequence is read as an independent batch entry of length L_n.)
  *   cu_seqlens       device [num_seqs+1] int32 (same values as the host copy)
  *   cu_seqlens_host  host   [num_seqs+1] int32, cu[0] = 0, non-decreasing;
  *                    used for validation and launch sizing (T = cu[num_seqs])
@@ -182,7 +186,11 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t *cfg, int32_t num_seqs,
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.  GDN_ERR_CUDA if the lookup
- *     fails.
+ *     fails.  Under lazy module loading (the CUDA default since 12.2) the
+ *     library's device code, this array with it, is loaded on that first
+ *     lookup, so the first call on each device can itself allocate device
+ *     memory and synchronise.  A caller that needs a steady state without
+ *     either makes one warm-up call per device at start-up.
  *   - Sharing: every call on a device uses the same array, which keeps the last
  *     call's contents.  Calls that can overlap on the GPU (different streams
  *     without ordering between them) race on it; order them.
@@ -218,6 +226,11 @@ gdn_status_t gdn_forward_verify(const gdn_config_t *cfg, int32_t batch, int32_t 
 
 /*
  * Commit an MTP round: sequence b keeps the first accepted[b] draft tokens.
+ * (mlxcel benchmark notes, "MTP speculative decoding": the target verifies a
+ * drafted block in one forward pass and keeps the accepted prefix, the
+ * "accepted draft tokens per verify"; the recurrent and conv states must then
+ * be those after the last accepted token, which this call restores from the
+ * verify's snapshots.)
  * accepted[b] = a in 1..L copies snapshot a-1 into the live conv and recurrent
  * states; a = 0 leaves them as they were before the verify.
  *   accepted  device [batch] int32

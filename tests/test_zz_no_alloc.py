@@ -5,7 +5,8 @@ device memory through its own pool, or a serving loop that may not touch the
 allocator (cudaMalloc can synchronise the device).  It runs the resident prefill
 with its workspace in a fixed device array inside the library.  These tests call
 it through the C ABI and compare it with gdn_forward_prefill, whose workspace
-comes from the caller, on two calls in a row with different inputs.  (This file
+comes from the caller, on two calls in a row with different inputs: both run the
+same kernels on the same inputs, so the results must agree bit for bit.  (This file
 sorts last so that a stop-at-first-failure run has already run every other test.)
 """
 import numpy as np
@@ -14,7 +15,7 @@ import torch
 
 from gated_deltanet_linear_causal_gb300 import binding as gb
 from gated_deltanet_linear_causal_gb300 import synth
-from gdn_testutil import assert_parity, configs, device, f64, to_dev
+from gdn_testutil import assert_parity, bits, configs, device, f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -51,8 +52,11 @@ def test_noalloc_matches_the_allocating_prefill_on_two_calls():
         gb.gdn_forward_prefill_noalloc(cfg, N, a["cu"], cu_host, a["qkv"], a["w"], a["gate"], a["beta"], conv, S,
                                        out)
         torch.cuda.synchronize()
+        # the same kernels on the same inputs, only the workspace address differs: bit for bit
+        assert np.array_equal(bits(out), bits(out_ref)), f"call {n}: output"
+        assert np.array_equal(bits(S), bits(S_ref)), f"call {n}: recurrent state"
+        assert np.array_equal(bits(conv), bits(conv_ref)), f"call {n}: conv state"
         assert_parity(f64(out), f64(out_ref), f64(S), f64(S_ref), what=f"call {n}")
-        assert torch.equal(conv, conv_ref)
 
 
 def test_noalloc_rejects_a_problem_larger_than_its_scratch():
