@@ -65,3 +65,28 @@ def configs(shape, io="bf16", use_l2=True, eps=1e-6):
     o = oracle.Cfg(shape.num_k_heads, shape.num_v_heads, shape.head_k_dim, shape.head_v_dim, shape.conv_kernel,
                    use_l2, eps)
     return g, o
+
+
+class Guarded:
+    """An output buffer with guard bands: the tensor handed to the library is the middle
+    of a larger allocation whose two ends hold a NaN pattern; check() fails if a kernel
+    wrote outside the buffer it was given."""
+
+    def __init__(self, shape, dtype, dev, guard_bytes=16384):
+        esize = torch.tensor([], dtype=dtype).element_size()
+        self.g = guard_bytes // esize
+        n = int(np.prod(shape))
+        self.buf = torch.empty(n + 2 * self.g, dtype=dtype, device=dev)
+        self.buf.fill_(float("nan"))
+        self.t = self.buf[self.g:self.g + n].view(shape)
+        self.head0 = bits(self.buf[:self.g]).copy()
+        self.tail0 = bits(self.buf[self.g + n:]).copy()
+
+    def fill_(self, value):
+        self.t.fill_(value)
+        return self
+
+    def check(self, what=""):
+        n = self.t.numel()
+        assert np.array_equal(bits(self.buf[:self.g]), self.head0), f"{what}: write below the buffer"
+        assert np.array_equal(bits(self.buf[self.g + n:]), self.tail0), f"{what}: write past the buffer"

@@ -6,7 +6,7 @@ import torch
 import oracle
 from gated_deltanet_linear_causal_gb300 import binding as gb
 from gated_deltanet_linear_causal_gb300 import synth
-from gdn_testutil import assert_parity, configs, device, f64, to_dev
+from gdn_testutil import Guarded, assert_parity, configs, device, f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +41,37 @@ def test_decode_oracle_scale_f32():
 def test_decode_production_b64_bf16():
     """The B=64, H_k=16, H_v=32, d=128 decode workload, three consecutive steps, every sequence checked."""
     _run_decode_steps(synth.PRODUCTION, "bf16", batch=64, steps=3, seed=2)
+
+
+def test_decode_production_256_steps_drift():
+    """The decode workload as timed: B=64, 256 consecutive steps on the same carried states.
+    Four sequences (every head) follow the oracle step by step: their outputs are compared at
+    every step and their fp32 states every 32 steps, so drift of the carried state over a long
+    decode run would show; the other sequences run alongside as in the bench."""
+    dev = device()
+    shape, B, steps, watch = synth.PRODUCTION, 64, 256, [0, 21, 42, 63]
+    cfg, ocfg = configs(shape, "bf16")
+    st = synth.decode_state(2, B, shape)
+    w_d, conv_d, S_d = to_dev(st["conv_weight"], dev), to_dev(st["conv_state"], dev), to_dev(st["ssm_state"], dev)
+    w64 = f64(st["conv_weight"])
+    conv_r, S_r = f64(st["conv_state"])[watch], st["ssm_state"][watch].astype(np.float64)
+    out = Guarded((B, shape.num_v_heads, shape.head_v_dim), torch.float32, dev)
+    worst = 0.0
+    for step in range(steps):
+        d = synth.decode_step(2, step, B, shape)
+        gb.gdn_forward_decode(cfg, B, to_dev(d["qkv"], dev), w_d, to_dev(d["gate"], dev), to_dev(d["beta"], dev),
+                              conv_d, S_d, out.t)
+        o_r, conv_r, S_r = oracle.decode(ocfg, f64(d["qkv"][watch]), w64, d["gate"][watch], d["beta"][watch],
+                                         conv_r, S_r)
+        o_g = f64(out.t[watch])
+        assert_parity(o_g, o_r, what=f"step {step} output")
+        if (step + 1) % 32 == 0:
+            S_g = f64(S_d[watch])
+            assert_parity(o_g, o_r, S_g, S_r, what=f"step {step} state")
+            worst = max(worst, float(np.linalg.norm(S_g - S_r) / np.linalg.norm(S_r)))
+    out.check("output")
+    assert np.array_equal(f64(conv_d[watch]), conv_r)
+    assert worst <= 1e-4
 
 
 @pytest.mark.parametrize("dk,dv,hk,hv", [(32, 32, 1, 1), (64, 64, 2, 2), (64, 96, 2, 8), (128, 64, 4, 16),

@@ -6,7 +6,8 @@ import torch
 import oracle
 from gated_deltanet_linear_causal_gb300 import binding as gb
 from gated_deltanet_linear_causal_gb300 import synth
-from gdn_testutil import assert_parity, bits, configs, device, f64, to_dev
+from gdn_testutil import Guarded, assert_parity, bits, configs, device, f64, to_dev
+from oracle_pool import heads_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -107,63 +108,69 @@ def test_prefill_split_equals_whole(cut):
         assert_parity(f64(out), f64(whole["out"]), f64(db["S"]), f64(whole["S"]), what="split vs whole")
 
 
-def _oracle_heads(ocfg, x, n, heads):
-    """Oracle outputs and final states of value heads `heads` of sequence n only
-    (heads are independent: each needs its key head's Q/K channels and its V channels)."""
-    Hk, Hv, dk, dv, K = ocfg.num_k_heads, ocfg.num_v_heads, ocfg.head_k_dim, ocfg.head_v_dim, ocfg.conv_kernel
-    f = Hv // Hk
-    cu = x["cu_seqlens"]
-    a, b = int(cu[n]), int(cu[n + 1])
-    sub = oracle.Cfg(1, 1, dk, dv, K, ocfg.use_qk_l2norm, ocfg.l2norm_eps)
-    res = {}
-    for h in heads:
-        hk = h // f
-        ch = np.r_[hk * dk:(hk + 1) * dk, Hk * dk + hk * dk:Hk * dk + (hk + 1) * dk,
-                   2 * Hk * dk + h * dv:2 * Hk * dk + (h + 1) * dv]
-        r = oracle.forward_sequence(sub, f64(x["qkv"][ch, a:b]), f64(x["conv_weight"][ch]),
-                                    f64(x["conv_state"][n][ch]), x["ssm_state"][n][h:h + 1],
-                                    x["gate"][a:b, h:h + 1], x["beta"][a:b, h:h + 1])
-        res[h] = (r["o"][:, 0], r["S"][0])
-    return res
-
-
 BOTH = [gb.GDN_PREFILL_RESIDENT, gb.GDN_PREFILL_CHUNKED]
 
 
-@pytest.mark.parametrize("variant", BOTH, ids=["resident", "chunked"])
-def test_prefill_long_production_sampled_heads(variant):
-    """B=1, L=8192, H_k=16, H_v=32, d=128, slow decay: the whole layer on the GPU;
-    the oracle recomputes value heads 0, 13 and 31 over the full sequence."""
-    dev = device()
-    shape = synth.PRODUCTION
-    cfg, ocfg = configs(shape, "bf16")
+@pytest.fixture(scope="module")
+def long_ref():
+    """The L=8192 workload and the oracle's result for every value head (one spawned
+    job per head)."""
+    _, ocfg = configs(synth.PRODUCTION, "bf16")
     x = synth.long_prefill(seed=3)
-    d = _prefill_dev(cfg, x, dev, variant, "bf16")
-    ref = _oracle_heads(ocfg, x, 0, [0, 13, 31])
-    torch.cuda.synchronize()
-    out, S = f64(d["out"]), f64(d["S"])
-    assert np.isfinite(out).all()
-    for h, (o_r, S_r) in ref.items():
-        assert_parity(out[:, h], o_r, S[0, h], S_r, what=f"head {h}")
-    tail = f64(x["qkv"][:, -3:])
-    assert np.array_equal(f64(d["conv"])[0], tail), "conv state = last K-1 raw inputs"
+    return x, heads_reference(ocfg, x, [(0, h) for h in range(synth.PRODUCTION.num_v_heads)])
+
+
+@pytest.fixture(scope="module")
+def varlen_ref():
+    """The 16-sequence packed workload and the oracle's result for every (sequence, head)."""
+    _, ocfg = configs(synth.PRODUCTION, "bf16")
+    x = synth.varlen_prefill(seed=4)
+    N = len(x["cu_seqlens"]) - 1
+    return x, heads_reference(ocfg, x, [(n, h) for n in range(N) for h in range(synth.PRODUCTION.num_v_heads)])
 
 
 @pytest.mark.parametrize("variant", BOTH, ids=["resident", "chunked"])
-def test_prefill_varlen_production_sampled(variant):
-    """16 sequences with lengths U{256..2048}, random per-sequence states: the oracle
-    recomputes 3 sequences x 3 value heads."""
+def test_prefill_long_production_all_heads(variant, long_ref):
+    """B=1, L=8192, H_k=16, H_v=32, d=128, slow decay: the whole layer on the GPU, every
+    value head's output and final state against the oracle, and the output buffer's guard
+    bands untouched."""
     dev = device()
     shape = synth.PRODUCTION
-    cfg, ocfg = configs(shape, "bf16")
-    x = synth.varlen_prefill(seed=4)
+    cfg, _ = configs(shape, "bf16")
+    x, ref = long_ref
+    cu = x["cu_seqlens"]
+    T = int(cu[-1])
+    conv, S = to_dev(x["conv_state"], dev), to_dev(x["ssm_state"], dev)
+    out = Guarded((T, shape.num_v_heads, shape.head_v_dim), torch.float32, dev)
+    ws = torch.empty(max(1, gb.gdn_prefill_workspace_size(cfg, 1, T, variant)), dtype=torch.uint8, device=dev)
+    gb.gdn_forward_prefill(cfg, 1, to_dev(cu, dev), cu, to_dev(x["qkv"], dev), to_dev(x["conv_weight"], dev),
+                           to_dev(x["gate"], dev), to_dev(x["beta"], dev), conv, S, out.t, variant, ws)
+    torch.cuda.synchronize()
+    o, Sg = f64(out.t), f64(S)
+    assert np.isfinite(o).all()
+    for h in range(shape.num_v_heads):
+        o_r, S_r = ref[(0, h)]
+        assert_parity(o[:, h], o_r, Sg[0, h], S_r, what=f"head {h}")
+    out.check("output")
+    tail = f64(x["qkv"][:, -3:])
+    assert np.array_equal(f64(conv)[0], tail), "conv state = last K-1 raw inputs"
+
+
+@pytest.mark.parametrize("variant", BOTH, ids=["resident", "chunked"])
+def test_prefill_varlen_production_all(variant, varlen_ref):
+    """16 sequences with lengths U{256..2048}, random per-sequence states: every sequence's
+    output, final state and conv state for every value head against the oracle."""
+    dev = device()
+    shape = synth.PRODUCTION
+    cfg, _ = configs(shape, "bf16")
+    x, ref = varlen_ref
     d = _prefill_dev(cfg, x, dev, variant, "bf16")
     torch.cuda.synchronize()
     out, S = f64(d["out"]), f64(d["S"])
     cu = x["cu_seqlens"]
-    for n in (0, 7, 15):
-        for h, (o_r, S_r) in _oracle_heads(ocfg, x, n, [1, 16, 30]).items():
-            assert_parity(out[cu[n]:cu[n + 1], h], o_r, S[n, h], S_r, what=f"seq {n} head {h}")
+    for (n, h), (o_r, S_r) in sorted(ref.items()):
+        assert_parity(out[cu[n]:cu[n + 1], h], o_r, S[n, h], S_r, what=f"seq {n} head {h}")
+    for n in range(len(cu) - 1):
         assert np.array_equal(f64(d["conv"])[n], f64(x["qkv"][:, cu[n + 1] - 3:cu[n + 1]]))
 
 
