@@ -52,16 +52,16 @@ def _source_sha(names):
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel_key, sources):
-    """Per-launch DRAM bytes from the committed ncu summary, or None if the kernel's
-    sources changed since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "stream_kernel_decode_b64.json")
+def _traffic(kernel_key, sources, profile="stream_kernel_decode_b64.json", field="dram_bytes_per_launch"):
+    """DRAM bytes per launch (or per call) from a committed ncu summary, or None if the
+    kernels' sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel_key)
     if not d or d.get("source_sha") != _source_sha(sources):
         return None
-    return d.get("dram_bytes_per_launch")
+    return d.get(field)
 
 
 class ClockSampler:
@@ -164,6 +164,33 @@ def prefill_bytes(shape, cu, random_state):
     conv = N * shape.D * (shape.conv_kernel - 1) * 2
     return (T * shape.D * 2 + T * shape.num_v_heads * shape.head_v_dim * 4 + 2 * T * shape.num_v_heads * 4 +
             shape.D * shape.conv_kernel * 2 + (2 if random_state else 1) * (S + conv))
+
+
+def chunked_tensor_flops(shape, cu, C=64):
+    """Tensor-core flops of one chunked prefill call (64-token chunks), as the products are
+    defined (algorithmic) and as issued (every product takes fp32 operands as bf16 hi/lo
+    pairs: three bf16 products each).  Per (chunk, key head): [K; Q] K^T; per (chunk,
+    value head): W = T diag(beta gamma) K and u = T diag(beta) V, then the chain's
+    [W; Q~] S0, K~^T U and [P; P] U (P stacked twice so that it accumulates onto the
+    Q~ S0 rows)."""
+    dk, dv, f = shape.head_k_dim, shape.head_v_dim, shape.num_v_heads // shape.num_k_heads
+    nchunk = sum((int(cu[i + 1]) - int(cu[i]) + C - 1) // C for i in range(len(cu) - 1))
+    gram = 2 * (2 * C) * C * dk
+    per_vhead = 2 * C * dk * C + 2 * C * dv * C + 2 * (2 * C) * dv * dk + 2 * dk * dv * C + 2 * (2 * C) * dv * C
+    per_pair = gram + f * per_vhead
+    issued = 3 * per_pair * nchunk * shape.num_k_heads
+    return issued // 3, issued
+
+
+def prefill_roofline(nbytes, flops_issued, ms, peaks):
+    """The larger of the HBM bound (algorithmic bytes / measured copy bandwidth) and the
+    tensor bound (issued flops / measured sustained bf16 rate) against the measured time."""
+    hbm_us = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    tensor_us = flops_issued / (peaks["bf16_tflops_sustained"] * 1e12) * 1e6
+    bound_us = max(hbm_us, tensor_us)
+    return {"hbm_bound_us": round(hbm_us, 2), "tensor_bound_us": round(tensor_us, 2),
+            "bound": "hbm" if hbm_us >= tensor_us else "tensor", "bound_us": round(bound_us, 2),
+            "frac": round(bound_us / (ms * 1e3), 4)}
 
 
 def verify_bytes(shape, B, L):
@@ -568,21 +595,29 @@ def main():
     sec = {}
     if secondary and rank == 0:
         shape = synth.PRODUCTION
+        chunk_sources = ["gdn_chunked.cu", "gdn_common.cuh", "gdn_tma.cuh", "gdn_umma.cuh"]
         for name, variant in (("chunked", gb.GDN_PREFILL_CHUNKED), ("resident", gb.GDN_PREFILL_RESIDENT)):
             key = "" if name == "chunked" else "_resident"
-            med, times = run_prefill(dev, x_long, variant)
-            nb = prefill_bytes(shape, x_long["cu_seqlens"], False)
-            sec["prefill_L8192" + key] = {"variant": name, "tokens_per_s": round(8192 / (med / 1e3), 1),
-                                          "ms": round(med, 4), "reps": len(times), "spread": _spread(times),
-                                          "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                          "algorithmic_bytes": nb, "cold_l2": True}
-            med, times = run_prefill(dev, x_var, variant)
-            T = int(x_var["cu_seqlens"][-1])
-            nb = prefill_bytes(shape, x_var["cu_seqlens"], True)
-            sec["prefill_varlen16" + key] = {"variant": name, "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1),
-                                             "ms": round(med, 4), "reps": len(times), "spread": _spread(times),
-                                             "roofline_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                             "algorithmic_bytes": nb, "cold_l2": True}
+            for label, x, rand in (("prefill_L8192", x_long, False), ("prefill_varlen16", x_var, True)):
+                med, times = run_prefill(dev, x, variant)
+                cu = x["cu_seqlens"]
+                T = int(cu[-1])
+                nb = prefill_bytes(shape, cu, rand)
+                e = {"variant": name, "tokens": T, "tokens_per_s": round(T / (med / 1e3), 1), "ms": round(med, 4),
+                     "reps": len(times), "spread": _spread(times),
+                     "hbm_frac": round(nb / (med / 1e3) / 1e9 / peaks["hbm_gbs"], 4), "algorithmic_bytes": nb,
+                     "cold_l2": True}
+                if name == "chunked":
+                    alg, issued = chunked_tensor_flops(shape, cu)
+                    r = prefill_roofline(nb, issued, med, peaks)
+                    e.update(algorithmic_tensor_flops=alg, issued_tensor_flops=issued, roofline=r,
+                             roofline_frac=r["frac"],
+                             traffic=_traffic(label.replace("prefill_", "prefill_chunked_"), chunk_sources,
+                                              "chunked_prefill_L8192.json", "dram_bytes_per_call")
+                             if label == "prefill_L8192" else None)
+                else:
+                    e["roofline_frac"] = e["hbm_frac"]  # bound by its serial chain; reported against HBM
+                sec[label + key] = e
         ms = run_decode_raw_gates(dev, st, steps)
         nb = decode_bytes(shape, B_DECODE) + 2 * 32 * 4
         sec["decode_B64_raw_gates"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),

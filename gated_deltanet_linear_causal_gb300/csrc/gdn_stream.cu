@@ -1,10 +1,13 @@
 // gdn_stream.cu -- decode and MTP verify as one persistent, TMA-fed kernel.
 //
-// Work item = (sequence b, key head hk): the f = Hv/Hk value heads that share
-// key head hk (reverse GQA, MNN "Qwen3.5" page, section 1.3).  Owning an item
+// Work item of decode = (sequence b, key head hk): the f = Hv/Hk value heads that
+// share key head hk (reverse GQA, MNN "Qwen3.5" page, section 1.3).  Owning an item
 // means owning every channel it reads, so the in-place conv-state rewrite has a
-// single reader/writer and needs no cross-CTA synchronisation.  One CTA per SM
-// walks its items with three warp-specialised roles:
+// single reader/writer and needs no cross-CTA synchronisation.  Verify writes its
+// conv states to separate snapshots, so its items are single value heads (b, h),
+// twice as many, which balances them better over the SMs; the Q/K conv snapshots
+// of key head hk are written by the item of its first value head only.  One CTA
+// per SM walks its items with three warp-specialised roles:
 //   producer (1 warp)  keeps a ring of shared-memory stages nstage tiles ahead:
 //                      each tile (dk rows x 128 columns of one value head's fp32
 //                      state) arrives by bulk asynchronous copy (cp.async.bulk,
@@ -16,9 +19,15 @@
 //                      (verify), then the L2 norms and the 1/sqrt(dk) scale;
 //   compute (8 warps)  runs Step 5, the gated delta rule, on each tile held in
 //                      registers, one token at a time, and stores the new state
-//                      (decode, in place) or every per-token snapshot (verify)
-//                      straight from registers; with the gated RMSNorm fused
-//                      (decode, dv = 128) it writes the normalised output instead.
+//                      (decode, in place) straight from registers, or every
+//                      per-token snapshot (verify): with dv = 128 a snapshot goes
+//                      into one of two shared-memory stages and leaves by bulk
+//                      asynchronous stores (cp.async.bulk) that eight lanes of
+//                      warp 0 issue once every warp has written its rows, so the
+//                      write stream proceeds beside the next token's arithmetic;
+//                      with the gated
+//                      RMSNorm fused (decode, dv = 128) it writes the normalised
+//                      output instead.
 // Every byte of state is read from HBM once and written once per token written.
 // Compute thread (warp w, lane l) holds columns 4l..4l+3 of rows w + 8m; the
 // reductions over dk go through shared memory in a fixed order, so decode and
@@ -44,7 +53,7 @@ constexpr int kProducerWarp = kComputeWarps + kPrologWarps;     // bulk copies i
 constexpr int kCompute = kComputeWarps * 32;
 constexpr int kProlog = kPrologWarps * 32;
 constexpr int kThreads = (kComputeWarps + kPrologWarps + 1) * 32;
-constexpr int kBarCompute = 1, kBarProlog = 2;                  // named barrier ids
+constexpr int kBarCompute = 1, kBarProlog = 2, kBarSnap = 3;    // named barrier ids
 constexpr int kTileCols = 128;
 constexpr int kStreamConv = 4;  // conv widths K <= 4 (the layer's K = 4) take this kernel
 
@@ -63,6 +72,11 @@ struct Tile {
     __device__ __forceinline__ void store_global(float* base, int dv) const {
 #pragma unroll
         for (int m = 0; m < RPT; ++m) st_stream(base + (size_t)row(m) * dv + col4(), s[m]);
+    }
+    // the held rows into a [DK][kTileCols] shared-memory stage
+    __device__ __forceinline__ void store_stage(float* stg) const {
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) *reinterpret_cast<float4*>(stg + row(m) * kTileCols + col4()) = s[m];
     }
 
     // One token of the gated delta rule on the tile (same algebra as
@@ -108,12 +122,14 @@ struct Tile {
     }
 };
 
-// Shared-memory carve-up (dynamic part).
+// Shared-memory carve-up (dynamic part).  snap: verify snapshots leave through
+// per-warp double-buffered stages of dk/8 rows (dv = 128).
 struct Layout {
-    size_t stage, qk, v, coef, ab, nred, red, zs, bars, total;
-    __host__ __device__ Layout(int DK, int nstage, int L, int f, int dv) {
+    size_t stage, snap, qk, v, coef, ab, nred, red, zs, bars, total;
+    __host__ __device__ Layout(int DK, int nstage, int L, int f, int dv, bool snap_stage) {
         size_t o = 0;
         stage = o; o += (size_t)nstage * DK * kTileCols * 4;
+        snap = o;  o += snap_stage ? (size_t)2 * DK * kTileCols * 4 : 0;  // two [DK][128] stages
         qk = o;    o += (size_t)2 * L * 2 * DK * 4;          // double-buffered by item
         v = o;     o += (size_t)2 * L * f * dv * 4;
         coef = o;  o += (size_t)2 * 3 * kMaxVerify * 4;
@@ -126,17 +142,36 @@ struct Layout {
     }
 };
 
-// Geometry of one item's tile r.
+// An item: sequence b, key head hk, its value heads h0 .. h0 + fi - 1 (fi = f for
+// the key-head items of decode, 1 for the value-head items of verify).
+struct ItemRef {
+    int b, hk, h0;
+};
+__device__ __forceinline__ ItemRef item_ref(const Geom& g, int item, bool per_vhead) {
+    ItemRef r;
+    if (per_vhead) {
+        r.b = item / g.Hv;
+        r.h0 = item % g.Hv;
+        r.hk = r.h0 / g.f;
+    } else {
+        r.b = item / g.Hk;
+        r.hk = item % g.Hk;
+        r.h0 = r.hk * g.f;
+    }
+    return r;
+}
+// Geometry of one item's tile r (hl: the tile's value head within the item).
 struct TileRef {
     int b, hk, h, hl, col0;
 };
-__device__ __forceinline__ TileRef tile_ref(const Geom& g, int item, int r) {
+__device__ __forceinline__ TileRef tile_ref(const Geom& g, int item, int r, bool per_vhead) {
     const int nsl = g.dv / kTileCols;
+    const ItemRef it = item_ref(g, item, per_vhead);
     TileRef t;
-    t.b = item / g.Hk;
-    t.hk = item % g.Hk;
+    t.b = it.b;
+    t.hk = it.hk;
     t.hl = r / nsl;
-    t.h = t.hk * g.f + t.hl;
+    t.h = it.h0 + t.hl;
     t.col0 = (r % nsl) * kTileCols;
     return t;
 }
@@ -177,7 +212,7 @@ __device__ __forceinline__ void norm_out(const NormParams& np, size_t at, float4
 // Separate instantiations keep the plain path unchanged.
 template <typename T, int DK, bool IN_PLACE, bool RAW, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, const int nstage, const GateParams gp,
-                                                             const NormParams np) {
+                                                             const NormParams np, const int snap_stage) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ int s_abort;    // any role gave up: the others stop waiting
     __shared__ int s_cabort;   // compute group's own flag (uniform decisions)
@@ -185,14 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
     const Geom& g = a.g;
     const int L = a.L;
     constexpr int TILE = DK * kTileCols;
-    const int tpi = g.f * (g.dv / kTileCols);  // tiles per item
-    const int nitems = a.B * g.Hk;
+    constexpr bool VI = !IN_PLACE;            // items are single value heads (verify)
+    const int fi = VI ? 1 : g.f;              // value heads per item
+    const int tpi = fi * (g.dv / kTileCols);  // tiles per item
+    const int nitems = a.B * (VI ? g.Hv : g.Hk);
     const int my_items = (nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int ntiles = my_items * tpi;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const Layout lay(DK, nstage, L, g.f, g.dv);
+    const Layout lay(DK, nstage, L, fi, g.dv, snap_stage != 0);
     float* stage = reinterpret_cast<float*>(smem_raw + lay.stage);
+    float* snap_buf = reinterpret_cast<float*>(smem_raw + lay.snap);
     float* qk_buf = reinterpret_cast<float*>(smem_raw + lay.qk);
     float* v_buf = reinterpret_cast<float*>(smem_raw + lay.v);
     float* coef_buf = reinterpret_cast<float*>(smem_raw + lay.coef);
@@ -241,21 +279,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 }
                 break;
             }
-            const TileRef tr = tile_ref(g, (int)blockIdx.x + (j / tpi) * (int)gridDim.x, j % tpi);
+            const TileRef tr = tile_ref(g, (int)blockIdx.x + (j / tpi) * (int)gridDim.x, j % tpi, VI);
             const float* src = a.S_in + ((size_t)(tr.b * g.Hv + tr.h) * DK) * g.dv + tr.col0;
             float* dst = stage + (size_t)s * TILE;
             // gated norm (dv == 128, one tile per value head): the item's z rides on its first
             // tile's barrier, into buffer item % (nstage + 1): the ring runs at most nstage
             // tiles, so fewer than nstage + 1 items, ahead of the oldest tile in use
             const bool zcopy = NORM && j % tpi == 0;
-            const uint32_t zbytes = (uint32_t)(g.f * g.dv * sizeof(T));
+            const uint32_t zbytes = (uint32_t)(fi * g.dv * sizeof(T));
             if (lane == 0) {
                 fence_proxy_async_smem();  // the compute warps' reads of this stage come first
                 mbar_arrive_expect_tx(full + s, TILE * 4 + (zcopy ? zbytes : 0));
                 if (g.dv == kTileCols) bulk_g2s(dst, src, TILE * 4, full + s);
                 if (zcopy)
-                    bulk_g2s(reinterpret_cast<T*>(zs_buf) + (size_t)((j / tpi) % (nstage + 1)) * g.f * g.dv,
-                             static_cast<const T*>(np.z) + ((size_t)tr.b * g.Hv + tr.hk * g.f) * g.dv, zbytes, full + s);
+                    bulk_g2s(reinterpret_cast<T*>(zs_buf) + (size_t)((j / tpi) % (nstage + 1)) * fi * g.dv,
+                             static_cast<const T*>(np.z) + ((size_t)tr.b * g.Hv + tr.h - tr.hl) * g.dv, zbytes, full + s);
             }
             if (g.dv != kTileCols) {
                 __syncwarp();
@@ -278,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
         const T* w = static_cast<const T*>(a.w);
         const T* cin = static_cast<const T*>(a.conv_in);
         T* cout = static_cast<T*>(a.conv_out);
-        const int nch = 2 * DK + g.f * g.dv;
+        const int nch = 2 * DK + fi * g.dv;
         for (int i = 0; i < my_items; ++i) {
             const int buf = i & 1;
             if (!mbar_wait_or_abort(qempty + buf, (uint32_t)(((i >> 1) & 1) ^ 1), &s_abort)) s_pabort = 1;
@@ -288,12 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 if (pt == 0) flag_device_error(&g_stream_error, 7);
                 return;
             }
-            const int item = (int)blockIdx.x + i * (int)gridDim.x;
-            const int b = item / g.Hk, hk = item % g.Hk;
+            const ItemRef it = item_ref(g, (int)blockIdx.x + i * (int)gridDim.x, VI);
+            const int b = it.b, hk = it.hk, h0 = it.h0;
+            // verify: the Q/K conv snapshots of key head hk come from its first value head's item
+            const bool qk_snap = !VI || h0 == hk * g.f;
             float* qk = qk_buf + (size_t)buf * L * 2 * DK;
-            float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
+            float* vv = v_buf + (size_t)buf * L * fi * g.dv;
             float* coef = coef_buf + buf * 3 * kMaxVerify;
-            float* ab = ab_buf + (size_t)buf * L * g.f * 2;
+            float* ab = ab_buf + (size_t)buf * L * fi * 2;
             // gate/beta of the item: the first values per thread
             // are loaded here and stored after the conv loop, so that their trip to
             // memory overlaps the conv inputs' instead of preceding it
@@ -303,9 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             for (int m = 0; m < kPG; ++m) {
                 const int idx = pt + m * kProlog;
                 pgv[m] = pbv[m] = 0.f;
-                if (idx < L * g.f) {
-                    const int t = idx / g.f, hl = idx - t * g.f;
-                    const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
+                if (idx < L * fi) {
+                    const int t = idx / fi, hl = idx - t * fi;
+                    const size_t gi = ((size_t)b * L + t) * g.Hv + h0 + hl;
                     pgv[m] = a.gate[gi];
                     pbv[m] = a.beta[gi];
                 }
@@ -321,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                     const int ch = ch0 + u;
                     cc[u] = ch < DK ? hk * DK + ch
                           : ch < 2 * DK ? g.Hk * DK + hk * DK + (ch - DK)
-                                        : 2 * g.Hk * DK + hk * g.f * g.dv + (ch - 2 * DK);
+                                        : 2 * g.Hk * DK + h0 * g.dv + (ch - 2 * DK);
                     win[u].load(cin + ((size_t)b * g.D + cc[u]) * (g.K - 1), w + (size_t)cc[u] * g.K, g.K);
                 }
                 for (int t = 0; t < L; ++t) {
@@ -333,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                         const int ch = ch0 + u;
                         const float y = win[u].push(xt[u]);
                         if (ch < 2 * DK) qk[t * 2 * DK + ch] = y;
-                        else vv[t * g.f * g.dv + (ch - 2 * DK)] = y;
-                        if (!IN_PLACE) win[u].store_state(cout + (((size_t)b * L + t) * g.D + cc[u]) * (g.K - 1), g.K);
+                        else vv[t * fi * g.dv + (ch - 2 * DK)] = y;
+                        if (!IN_PLACE && (qk_snap || ch >= 2 * DK))
+                            win[u].store_state(cout + (((size_t)b * L + t) * g.D + cc[u]) * (g.K - 1), g.K);
                     }
                 }
                 if (IN_PLACE) {
@@ -343,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 }
             }
             auto put_ab = [&](int idx, float gv, float bv) {
-                const int hl = idx % g.f;
+                const int hl = idx % fi;
                 if (RAW) {
-                    ab[2 * idx + 0] = expf(gate_of(gp.A_log, gp.dt_bias, gv, hk * g.f + hl));
+                    ab[2 * idx + 0] = expf(gate_of(gp.A_log, gp.dt_bias, gv, h0 + hl));
                     ab[2 * idx + 1] = beta_of(gp.A_log, bv);
                 } else {
                     ab[2 * idx + 0] = expf(gv);
@@ -354,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             };
 #pragma unroll
             for (int m = 0; m < kPG; ++m)
-                if (pt + m * kProlog < L * g.f) put_ab(pt + m * kProlog, pgv[m], pbv[m]);
-            for (int idx = pt + kPG * kProlog; idx < L * g.f; idx += kProlog) {
-                const int t = idx / g.f, hl = idx - t * g.f;
-                const size_t gi = ((size_t)b * L + t) * g.Hv + hk * g.f + hl;
+                if (pt + m * kProlog < L * fi) put_ab(pt + m * kProlog, pgv[m], pbv[m]);
+            for (int idx = pt + kPG * kProlog; idx < L * fi; idx += kProlog) {
+                const int t = idx / fi, hl = idx - t * fi;
+                const size_t gi = ((size_t)b * L + t) * g.Hv + h0 + hl;
                 put_ab(idx, a.gate[gi], a.beta[gi]);
             }
             named_sync(kBarProlog, kProlog);
@@ -409,14 +450,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
     }
 
     // ---- compute: step 5 on every tile of every item ----
-    int ustep = 0;  // running token-step counter: alternates the reduction buffers
+    int ustep = 0;  // running token-step counter: alternates the reduction buffers and snapshot stages
+    const bool staged = !IN_PLACE && snap_stage;
+    // a snapshot stage, once every warp has written its rows (warps 1-7 arrive on kBarSnap,
+    // warp 0 waits there), leaves by eight bulk stores issued by lanes j < 8 of warp 0,
+    // rows j*dk/8 .. +dk/8-1; each lane then waits until its previous store (from the
+    // other stage) has read its rows, before warp 0 reaches the next token's reduction
+    // barrier, i.e. before any warp writes that stage again
+    constexpr int kSnapRows = DK / kComputeWarps;
     for (int i = 0; i < my_items; ++i) {
         const int buf = i & 1;
         if (!mbar_wait_or_abort(qfull + buf, (uint32_t)((i >> 1) & 1), &s_abort)) s_cabort = 1;
         const float* qk = qk_buf + (size_t)buf * L * 2 * DK;
-        const float* vv = v_buf + (size_t)buf * L * g.f * g.dv;
+        const float* vv = v_buf + (size_t)buf * L * fi * g.dv;
         const float* coef = coef_buf + buf * 3 * kMaxVerify;
-        const float* ab = ab_buf + (size_t)buf * L * g.f * 2;
+        const float* ab = ab_buf + (size_t)buf * L * fi * 2;
         for (int r = 0; r < tpi; ++r) {
             const int j = i * tpi + r, s = j % nstage;
             if (!mbar_wait_or_abort(full + s, (uint32_t)((j / nstage) & 1), &s_abort)) s_cabort = 1;
@@ -424,34 +472,55 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
             if (s_cabort) {
                 s_abort = 1;
                 if (tid == 0) flag_device_error(&g_stream_error, 7);
+                if (staged && warp == 0 && lane < kComputeWarps) bulk_wait_all();  // stores still reading the stages
                 return;
             }
-            const TileRef tr = tile_ref(g, (int)blockIdx.x + i * (int)gridDim.x, r);
+            const TileRef tr = tile_ref(g, (int)blockIdx.x + i * (int)gridDim.x, r, VI);
             Tile<DK> S;
             S.load_smem(stage + (size_t)s * TILE);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + s);
             for (int t = 0; t < L; ++t) {
                 const size_t gi = ((size_t)tr.b * L + t) * g.Hv + tr.h;
-                const float alpha = ab[2 * (t * g.f + tr.hl) + 0];
-                const float bt = ab[2 * (t * g.f + tr.hl) + 1];
+                const float alpha = ab[2 * (t * fi + tr.hl) + 0];
+                const float bt = ab[2 * (t * fi + tr.hl) + 1];
                 const float4 v4 =
-                    *reinterpret_cast<const float4*>(vv + t * g.f * g.dv + tr.hl * g.dv + tr.col0 + Tile<DK>::col4());
+                    *reinterpret_cast<const float4*>(vv + t * fi * g.dv + tr.hl * g.dv + tr.col0 + Tile<DK>::col4());
                 const float4 o = S.step(qk + t * 2 * DK + DK, qk + t * 2 * DK, v4, alpha, bt, coef[3 * t + 2],
                                         red + (ustep & 1) * kComputeWarps * 256);
+                const int sbuf = ustep & 1;
                 ++ustep;
                 if (NORM)
                     norm_out<T>(np, gi * g.dv, o, g.dv,
-                                reinterpret_cast<const T*>(zs_buf) + (size_t)(i % (nstage + 1)) * g.f * g.dv +
+                                reinterpret_cast<const T*>(zs_buf) + (size_t)(i % (nstage + 1)) * fi * g.dv +
                                     tr.hl * g.dv);
                 else if (warp == 0) st_stream(a.out + gi * g.dv + tr.col0 + Tile<DK>::col4(), o);
-                if (!IN_PLACE) S.store_global(a.S_out + (gi * DK) * g.dv + tr.col0, g.dv);
+                if (staged) {
+                    float* stg = snap_buf + (size_t)sbuf * DK * kTileCols;
+                    S.store_stage(stg);
+                    fence_proxy_async_smem();
+                    if (warp != 0) {
+                        named_arrive(kBarSnap, kCompute);
+                    } else {
+                        named_sync(kBarSnap, kCompute);
+                        if (lane < kComputeWarps) {
+                            const size_t r0 = (size_t)lane * kSnapRows;
+                            bulk_s2g(a.S_out + (gi * DK + r0) * g.dv, stg + r0 * kTileCols,
+                                     kSnapRows * kTileCols * 4);
+                            bulk_commit();
+                            bulk_wait_read<1>();
+                        }
+                    }
+                } else if (!IN_PLACE) {
+                    S.store_global(a.S_out + (gi * DK) * g.dv + tr.col0, g.dv);
+                }
             }
             if (IN_PLACE) S.store_global(a.S_out + ((size_t)(tr.b * g.Hv + tr.h) * DK) * g.dv + tr.col0, g.dv);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty + buf);  // this warp is done with the item's q/k/v
     }
+    if (staged && warp == 0 && lane < kComputeWarps) bulk_wait_all();  // every snapshot store has landed
 }
 
 int sm_count() {
@@ -468,14 +537,14 @@ int sm_count() {
 
 template <typename T, int DK, bool IN_PLACE>
 cudaError_t launch_t(const StepArgs& a, const GateParams& gp, const NormParams& np, int nstage, size_t smem,
-                     cudaStream_t stream) {
+                     int snap_stage, cudaStream_t stream) {
     auto kern = gp.A_log ? stream_kernel<T, DK, IN_PLACE, true, false> : stream_kernel<T, DK, IN_PLACE, false, false>;
     if constexpr (IN_PLACE) {
         if (np.z) kern = gp.A_log ? stream_kernel<T, DK, true, true, true> : stream_kernel<T, DK, true, false, true>;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int nitems = a.B * a.g.Hk;
+    const int nitems = a.B * (IN_PLACE ? a.g.Hk : a.g.Hv);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(nitems, sm_count()));
     cfg.blockDim = dim3(kThreads);
@@ -486,17 +555,21 @@ cudaError_t launch_t(const StepArgs& a, const GateParams& gp, const NormParams& 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, nstage, gp, np);
+    return cudaLaunchKernelEx(&cfg, kern, a, nstage, gp, np, snap_stage);
 }
 
 }  // namespace
 
-bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out) {
+// Ring depth and shared memory of a launch: with snapshot stages (verify, dv = 128) the
+// deepest ring that fits beside them (one stage is enough: a verify tile is held for L
+// token steps while the next one loads), else the deepest of at least two.
+namespace {
+bool stream_layout(const StepArgs& a, bool in_place, bool snap_stage, int* nstage_out, size_t* smem_out) {
     const Geom& g = a.g;
     if (g.dv % kTileCols != 0 || (g.dk != 64 && g.dk != 128) || g.K > kStreamConv) return false;
     const int max_stage = g.dk == 64 ? 4 : 3;
-    for (int ns = max_stage; ns >= 2; --ns) {
-        const size_t bytes = Layout(g.dk, ns, a.L, g.f, g.dv).total;
+    for (int ns = max_stage; ns >= (snap_stage ? 1 : 2); --ns) {
+        const size_t bytes = Layout(g.dk, ns, a.L, in_place ? g.f : 1, g.dv, snap_stage).total;
         if (bytes <= 227 * 1024 - 256) {
             *nstage_out = ns;
             *smem_out = bytes;
@@ -505,22 +578,33 @@ bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out)
     }
     return false;
 }
+}  // namespace
+
+bool stream_step_supported(const StepArgs& a, int* nstage_out, size_t* smem_out) {
+    return stream_layout(a, true, false, nstage_out, smem_out);
+}
 
 cudaError_t launch_stream_step(const StepArgs& a, const GateParams& gp, bool in_place, cudaStream_t s,
                                const NormParams& np) {
     if (np.z && (!in_place || a.g.dv != kTileCols)) return cudaErrorInvalidValue;
     int ns = 0;
     size_t smem = 0;
-    if (!stream_step_supported(a, &ns, &smem)) return cudaErrorInvalidValue;
+    int snap = !in_place && a.g.dv == kTileCols;
+    if (!snap || !stream_layout(a, in_place, true, &ns, &smem)) {
+        snap = 0;
+        if (!stream_layout(a, in_place, false, &ns, &smem)) return cudaErrorInvalidValue;
+    }
     const bool bf = a.g.io_bf16;
     if (a.g.dk == 128) {
-        if (bf) return in_place ? launch_t<__nv_bfloat16, 128, true>(a, gp, np, ns, smem, s)
-                                : launch_t<__nv_bfloat16, 128, false>(a, gp, np, ns, smem, s);
-        return in_place ? launch_t<float, 128, true>(a, gp, np, ns, smem, s) : launch_t<float, 128, false>(a, gp, np, ns, smem, s);
+        if (bf) return in_place ? launch_t<__nv_bfloat16, 128, true>(a, gp, np, ns, smem, snap, s)
+                                : launch_t<__nv_bfloat16, 128, false>(a, gp, np, ns, smem, snap, s);
+        return in_place ? launch_t<float, 128, true>(a, gp, np, ns, smem, snap, s)
+                        : launch_t<float, 128, false>(a, gp, np, ns, smem, snap, s);
     }
-    if (bf) return in_place ? launch_t<__nv_bfloat16, 64, true>(a, gp, np, ns, smem, s)
-                            : launch_t<__nv_bfloat16, 64, false>(a, gp, np, ns, smem, s);
-    return in_place ? launch_t<float, 64, true>(a, gp, np, ns, smem, s) : launch_t<float, 64, false>(a, gp, np, ns, smem, s);
+    if (bf) return in_place ? launch_t<__nv_bfloat16, 64, true>(a, gp, np, ns, smem, snap, s)
+                            : launch_t<__nv_bfloat16, 64, false>(a, gp, np, ns, smem, snap, s);
+    return in_place ? launch_t<float, 64, true>(a, gp, np, ns, smem, snap, s)
+                    : launch_t<float, 64, false>(a, gp, np, ns, smem, snap, s);
 }
 
 cudaError_t stream_error_read(int32_t* value, bool clear) {
