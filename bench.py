@@ -457,6 +457,49 @@ def run_prefill(dev, x, variant, reps=20):
     return med, times
 
 
+def run_prefill_gated(dev, x, variant, reps=20):
+    """The prefill with the gated RMSNorm fused (bf16 z in, bf16 y out), and the same
+    through gdn_forward_prefill then gdn_gated_rmsnorm; returns both median times."""
+    import torch
+    from gated_deltanet_linear_causal_gb300 import binding as gb, synth
+    shape = x["shape"]
+    cfg = gb.make_config(shape.num_k_heads, shape.num_v_heads, shape.head_k_dim, shape.head_v_dim, 4, True, 1e-6,
+                         "bf16")
+    cu = x["cu_seqlens"]
+    N, T = len(cu) - 1, int(cu[-1])
+    H, dv = shape.num_v_heads, shape.head_v_dim
+    d = synth.Draw(9)
+    cu_d = _to_dev(cu, dev)
+    qkv, w = _to_dev(x["qkv"], dev), _to_dev(x["conv_weight"], dev)
+    gate, beta = _to_dev(x["gate"], dev), _to_dev(x["beta"], dev)
+    conv0, S0 = _to_dev(x["conv_state"], dev), _to_dev(x["ssm_state"], dev)
+    conv, S = conv0.clone(), S0.clone()
+    z = _to_dev(d.bf16("z", (T, H, dv)), dev)
+    w_n = _to_dev(d.f32("norm_w", (dv,), 1.0, 0.3), dev)
+    y = torch.empty(T, H, dv, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(T, H, dv, device=dev)
+    ws = torch.empty(max(1, gb.gdn_prefill_workspace_size(cfg, N, T, variant)), dtype=torch.uint8, device=dev)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        conv.copy_(conv0)
+        S.copy_(S0)
+        scratch.zero_()
+
+    def fused():
+        gb.gdn_forward_prefill_gated(cfg, N, cu_d, cu, qkv, w, gate, beta, conv, S, z, w_n, 1e-6, y, variant, ws)
+
+    def unfused():
+        gb.gdn_forward_prefill(cfg, N, cu_d, cu, qkv, w, gate, beta, conv, S, out, variant, ws)
+        gb.gdn_gated_rmsnorm(cfg, T * H, out, z, w_n, 1e-6, y)
+
+    res = []
+    for fn in (fused, unfused):
+        fn()
+        res.append(_time_calls(fn, reps, flush))
+    return res
+
+
 def run_verify(dev, x, reps=20):
     import torch
     from gated_deltanet_linear_causal_gb300 import binding as gb
@@ -618,6 +661,12 @@ def main():
                 else:
                     e["roofline_frac"] = e["hbm_frac"]  # bound by its serial chain; reported against HBM
                 sec[label + key] = e
+        (mf, tf), (mu, _) = run_prefill_gated(dev, x_long, gb.GDN_PREFILL_CHUNKED)
+        sec["prefill_L8192_gated_norm"] = {"variant": "chunked", "tokens_per_s": round(8192 / (mf / 1e3), 1),
+                                           "ms": round(mf, 4), "reps": len(tf), "spread": _spread(tf),
+                                           "ms_prefill_then_norm_kernel": round(mu, 4), "cold_l2": True,
+                                           "note": "gated RMSNorm fused into the chain's output epilogue: bf16 z in, "
+                                                   "bf16 y out, no fp32 output written"}
         ms = run_decode_raw_gates(dev, st, steps)
         nb = decode_bytes(shape, B_DECODE) + 2 * 32 * 4
         sec["decode_B64_raw_gates"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),

@@ -26,7 +26,7 @@ GDN_PREFILL_RESIDENT, GDN_PREFILL_CHUNKED = 0, 1
 
 EXPORTED = ("gdn_conv_state_init", "gdn_forward_decode", "gdn_prefill_workspace_size", "gdn_forward_prefill",
             "gdn_forward_verify", "gdn_verify_commit", "gdn_status_string", "gdn_last_cuda_error",
-            "gdn_device_error", "gdn_gated_rmsnorm", "gdn_forward_decode_gated")
+            "gdn_device_error", "gdn_gated_rmsnorm", "gdn_forward_decode_gated", "gdn_forward_prefill_gated")
 
 
 class GdnError(RuntimeError):
@@ -104,8 +104,10 @@ def load(path: str | None = None):
         lib.gdn_device_error.restype = i32
         lib.gdn_gated_rmsnorm.argtypes = [cfgp, i64, vp, vp, vp, ctypes.c_float, vp, vp]
         lib.gdn_forward_decode_gated.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp]
+        lib.gdn_forward_prefill_gated.argtypes = [cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                                  vp, i32, vp, st, vp]
         for name in ("gdn_conv_state_init", "gdn_forward_decode", "gdn_forward_prefill", "gdn_forward_verify",
-                     "gdn_verify_commit", "gdn_gated_rmsnorm", "gdn_forward_decode_gated"):
+                     "gdn_verify_commit", "gdn_gated_rmsnorm", "gdn_forward_decode_gated", "gdn_forward_prefill_gated"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -223,6 +225,34 @@ def gdn_forward_prefill(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_we
     ws_bytes = workspace.numel() if workspace is not None else 0
     _check("gdn_forward_prefill", load().gdn_forward_prefill(ctypes.byref(cfg), num_seqs, *args, variant, ws_ptr,
                                                              ws_bytes, _stream(stream)))
+
+
+def gdn_forward_prefill_gated(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_weight, gate, beta, conv_state,
+                              ssm_state, z, norm_weight, norm_eps, y, variant=GDN_PREFILL_RESIDENT, workspace=None,
+                              stream=None):
+    """gdn_forward_prefill with the gated RMSNorm fused into the output: y (io dtype
+    [T, Hv, dv]) from z (io dtype [T, Hv, dv]) instead of the fp32 output."""
+    host = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous()
+    if host.is_cuda or host.numel() < num_seqs + 1:
+        raise ValueError("cu_seqlens_host: host int32 tensor of num_seqs+1 entries")
+    T = int(host[num_seqs]) if num_seqs > 0 else 0
+    if T == 0:
+        return
+    D, K, H, dv = cfg.D, cfg.conv_kernel, cfg.num_v_heads, cfg.head_v_dim
+    io = cfg.torch_dtype
+    ws_need = gdn_prefill_workspace_size(cfg, num_seqs, T, variant)
+    ws_ptr = _dev("workspace", workspace, torch.uint8, ws_need, optional=ws_need == 0)
+    args = [_dev("cu_seqlens", cu_seqlens, torch.int32, num_seqs + 1), host.data_ptr(),
+            _dev("qkv", qkv, io, D * T), _dev("conv_weight", conv_weight, io, D * K),
+            _dev("gate", gate, torch.float32, T * H), _dev("beta", beta, torch.float32, T * H),
+            _dev("conv_state", conv_state, io, num_seqs * D * (K - 1)),
+            _dev("ssm_state", ssm_state, torch.float32, num_seqs * H * cfg.head_k_dim * dv),
+            _dev("z", z, io, T * H * dv), _dev("norm_weight", norm_weight, torch.float32, dv)]
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check("gdn_forward_prefill_gated",
+           load().gdn_forward_prefill_gated(ctypes.byref(cfg), num_seqs, *args, float(norm_eps),
+                                            _dev("y", y, io, T * H * dv), variant, ws_ptr, ws_bytes,
+                                            _stream(stream)))
 
 
 def gdn_forward_verify(cfg, batch, L, qkv, conv_weight, gate, beta, conv_state, ssm_state, conv_snap, ssm_snap, out,

@@ -78,11 +78,13 @@ int32_t gdn_last_cuda_error(void) { return g_last_cuda_error; }
 
 gdn_status_t gdn_device_error(int32_t* value, int32_t clear) {
     if (!value) return GDN_ERR_NULL;
-    int32_t a = 0, b = 0;
+    int32_t a = 0, b = 0, c = 0;
     gdn_status_t st = cuda_status(gdn::stream_error_read(&a, clear != 0));
     if (st != GDN_OK) return st;
     st = cuda_status(gdn::chunk_error_read(&b, clear != 0));
-    *value = a ? a : b;
+    if (st != GDN_OK) return st;
+    st = cuda_status(gdn::prefill_error_read(&c, clear != 0));
+    *value = a ? a : b ? b : c;
     return st;
 }
 
@@ -265,10 +267,13 @@ size_t gdn_prefill_workspace_size(const gdn_config_t* cfg, int32_t num_seqs, int
     return 0;
 }
 
-gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, const int32_t* cu_seqlens,
-                                 const int32_t* cu_seqlens_host, const void* qkv, const void* conv_weight,
-                                 const float* gate, const float* beta, void* conv_state, float* ssm_state, float* out,
-                                 int32_t variant, void* workspace, size_t workspace_bytes, gdn_stream_t stream) {
+namespace {
+// Shared by gdn_forward_prefill and gdn_forward_prefill_gated: np.z set writes the
+// gated-RMSNorm output y instead of out.
+gdn_status_t prefill_call(const gdn_config_t* cfg, int32_t num_seqs, const int32_t* cu_seqlens,
+                          const int32_t* cu_seqlens_host, const void* qkv, const void* conv_weight, const float* gate,
+                          const float* beta, void* conv_state, float* ssm_state, float* out, int32_t variant,
+                          void* workspace, size_t workspace_bytes, gdn_stream_t stream, const gdn::NormParams& np) {
     gdn::Geom g;
     gdn_status_t st = check_config(cfg, &g);
     if (st != GDN_OK) return st;
@@ -286,10 +291,14 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, cons
     const int64_t T = cu_seqlens_host[num_seqs];
     if (T == 0) return GDN_OK;
     if (variant == GDN_PREFILL_CHUNKED && !gdn::prefill_chunked_supported(g)) return GDN_ERR_UNSUPPORTED;
-    if (!qkv || !conv_weight || !gate || !beta || (!conv_state && g.K > 1) || !ssm_state || !out) return GDN_ERR_NULL;
+    if (np.z && !gdn::prefill_norm_supported(g, variant)) return GDN_ERR_UNSUPPORTED;
+    if (!qkv || !conv_weight || !gate || !beta || (!conv_state && g.K > 1) || !ssm_state || (!out && !np.z))
+        return GDN_ERR_NULL;
+    if (np.z && (!np.weight || !np.y)) return GDN_ERR_NULL;
     const size_t eb = elem_bytes(cfg);
     if (!aligned(cu_seqlens, 4) || !aligned(qkv, 16) || !aligned(ssm_state, 16) || !aligned(out, 16) ||
-        !aligned(conv_weight, eb) || !aligned(conv_state, eb) || !aligned(gate, 4) || !aligned(beta, 4))
+        !aligned(conv_weight, eb) || !aligned(conv_state, eb) || !aligned(gate, 4) || !aligned(beta, 4) ||
+        !aligned(np.z, 16) || !aligned(np.y, 16) || !aligned(np.weight, 16))
         return GDN_ERR_ALIGN;
     const size_t need = gdn_prefill_workspace_size(cfg, num_seqs, T, variant);
     if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
@@ -310,10 +319,33 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, cons
     a.out = out;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
+    a.norm = np;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const gdn::GateParams gp{cfg->A_log, cfg->dt_bias};
     return cuda_status(variant == GDN_PREFILL_CHUNKED ? gdn::launch_prefill_chunked(a, gp, s)
                                                       : gdn::launch_prefill_resident(a, gp, s));
+}
+}  // namespace
+
+gdn_status_t gdn_forward_prefill(const gdn_config_t* cfg, int32_t num_seqs, const int32_t* cu_seqlens,
+                                 const int32_t* cu_seqlens_host, const void* qkv, const void* conv_weight,
+                                 const float* gate, const float* beta, void* conv_state, float* ssm_state, float* out,
+                                 int32_t variant, void* workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    return prefill_call(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_weight, gate, beta, conv_state,
+                        ssm_state, out, variant, workspace, workspace_bytes, stream, gdn::NormParams{});
+}
+
+gdn_status_t gdn_forward_prefill_gated(const gdn_config_t* cfg, int32_t num_seqs, const int32_t* cu_seqlens,
+                                       const int32_t* cu_seqlens_host, const void* qkv, const void* conv_weight,
+                                       const float* gate, const float* beta, void* conv_state, float* ssm_state,
+                                       const void* z, const float* norm_weight, float norm_eps, void* y,
+                                       int32_t variant, void* workspace, size_t workspace_bytes,
+                                       gdn_stream_t stream) {
+    if (!(norm_eps >= 0.f) || !std::isfinite(norm_eps)) return GDN_ERR_SHAPE;
+    if (!z || !norm_weight || !y) return GDN_ERR_NULL;
+    return prefill_call(cfg, num_seqs, cu_seqlens, cu_seqlens_host, qkv, conv_weight, gate, beta, conv_state,
+                        ssm_state, nullptr, variant, workspace, workspace_bytes, stream,
+                        gdn::NormParams{z, norm_weight, norm_eps, y});
 }
 
 }  // extern "C"

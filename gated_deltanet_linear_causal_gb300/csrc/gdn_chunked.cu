@@ -49,6 +49,7 @@ constexpr int kKC = 4;      // widest conv handled here
 constexpr int kMaxF = 16;   // value heads per key head
 constexpr int kPT = 512;    // chunk-prep threads
 constexpr int kCT = 160;    // chain threads: 4 epilogue warps (one state row each) + the MMA issuer's warp
+constexpr int kCTN = 256;   // with the fused norm: + an idle warp and the two output-row warps 6-7
 constexpr int kIssuer = 128;  // the chain thread that issues the MMAs
 constexpr uint32_t kImgBytes = kC * 2 * kDK * 2;  // split [64 tokens][2*128] image: 32 KB
 constexpr uint32_t kPBytes = kC * 2 * kC * 2;     // split [64][2*64] image: 16 KB
@@ -703,6 +704,43 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     if (warp == 0) umma::tmem_free(s_tmem, 512);
 }
 
+// 32 consecutive values of the io type (16-byte aligned) to and from fp32.
+// The 32 values of a row of io type T held as raw 16-byte words (4 for bf16, 8 for fp32).
+template <typename T>
+__device__ __forceinline__ void unpack_row32(const uint4 (&r)[32 * sizeof(T) / 16], float (&v)[32]) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bf16x8(r[q], v + 8 * q);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            v[4 * q] = __uint_as_float(r[q].x);
+            v[4 * q + 1] = __uint_as_float(r[q].y);
+            v[4 * q + 2] = __uint_as_float(r[q].z);
+            v[4 * q + 3] = __uint_as_float(r[q].w);
+        }
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store_row32(T* p, const float (&v)[32]) {
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(p + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(p + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+}
+
 // ---- chain ----------------------------------------------------------------------
 // A product accumulated by umma::mma_split_bpair: the sum of its two 32-column halves.
 __device__ __forceinline__ void tmem_pair(uint32_t taddr, float (&v)[kNS]) {
@@ -727,8 +765,25 @@ __device__ __forceinline__ void tmem_pair(uint32_t taddr, float (&v)[kNS]) {
 // issuer never waits on them): W/Q~ double-buffered two chunks ahead (free once round A of
 // the chunk before has completed), K~ once K~^T U has completed, u once the U
 // rows have been read, and P (twice, for the stacked operand) once P U has.
-template <typename T>
-__global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, const int32_t* __restrict__ coff,
+// NORM: the gated RMSNorm of section 2 is applied to the output rows.  That work
+// (sums of squares, SiLU of z, the stores) is too long for warps 2-3's share of round
+// A, so warps 6-7 (the same TMEM lanes) take the output rows instead, outside the
+// chain's barriers: they wait for O of chunk cc on s_on[cc & 1] and release its TMEM
+// buffer on s_oc[cc & 1], which the issuer waits for before round A of chunk cc + 2.
+// Each row's sum of squares runs over all dv columns: the dv/32 CTAs of a value head
+// form a cluster, and after reading a chunk's rows each output thread sends its
+// row's partial sum to every CTA of the cluster (asynchronous stores into their
+// shared memory that complete bytes on their barriers).  A chunk's rows are
+// normalised and stored one chunk later, by when the partials have arrived, so the
+// exchange never waits in the chain; the raw rows wait in registers, and the z rows
+// they need are loaded into registers (as raw bytes, converted at use, so that no
+// thread waits on the load) one chunk ahead.  Each step reads the
+// previous chunk's sums first, then sends this chunk's partials, then stores the
+// previous chunk's rows: a peer writes a partial buffer again only after the reads
+// of its previous use (the sends are ordered after them), and no send waits behind
+// this thread's global stores.
+template <typename T, bool NORM>
+__global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const PrefillArgs a, const int32_t* __restrict__ coff,
                                                        const ChunkOut ws) {
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* wqb = smem;                        // 2 x 64 KB: [W; Q~] images
@@ -741,6 +796,11 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_wq[2], s_u, s_k, s_p, s_a, s_s, s_o;
     __shared__ int s_abort;
+    // NORM: row sums of squares of a chunk from each CTA of the cluster, by chunk parity
+    __shared__ float s_np[NORM ? 2 : 1][NORM ? kMaxDV / kNS : 1][kC];
+    __shared__ __align__(8) uint64_t s_nb[2];
+    __shared__ float s_nw[NORM ? kNS : 1];  // the norm weights of this CTA's columns
+    __shared__ __align__(8) uint64_t s_on[2], s_oc[2];  // NORM: O of a chunk ready / read, by TMEM buffer
     const Geom& g = a.g;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int col0 = slice * kNS, nsl = g.dv / kNS;
@@ -754,7 +814,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         T* cst = static_cast<T*>(a.conv_state);
         const T* qkv = static_cast<const T*>(a.qkv);
         if (len > 0)
-            for (int c = r * per + tid; c < min(g.D, (r + 1) * per); c += kCT) {
+            for (int c = r * per + tid; c < min(g.D, (r + 1) * per); c += blockDim.x) {
                 T* st = cst + ((size_t)n * g.D + c) * (g.K - 1);
                 for (int i = 0; i < g.K - 1; ++i) {
                     const int p = len + i;
@@ -789,8 +849,23 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         mbar_init(&s_a, 1);
         mbar_init(&s_s, 1);
         mbar_init(&s_o, 1);
+        if (NORM) {
+            mbar_init(&s_nb[0], 1);  // one local arrive.expect_tx; the bytes come from the whole cluster
+            mbar_init(&s_nb[1], 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&s_on[b], 1);   // a commit of the issuer
+                mbar_init(&s_oc[b], 64);  // the 64 threads of warps 6-7
+            }
+        }
+    }
+    if (NORM && tid < kNS) s_nw[tid] = a.norm.weight[col0 + tid];
+    if (tid == 0) {
         fence_mbar_init();
         s_abort = 0;
+    }
+    if (NORM) {  // every CTA's barriers are initialised before any remote arrive
+        cluster_arrive_release();
+        cluster_wait_acquire();
     }
     fence_proxy_async_smem();  // S0 image written by the generic proxy
     umma::fence_before_sync();
@@ -832,6 +907,37 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
         if (!mbar_wait_bounded(bar, parity)) s_abort = 1;
     };
+    // NORM: the raw row of chunk prev_c held by this output thread, its z row (io type bytes)
+    float o_prev[kNS];
+    uint4 z_raw[kNS * sizeof(T) / 16];
+    int prev_c = -1;
+    const uint32_t crank = NORM ? cluster_ctarank() : 0;
+    // 1/RMS of row t of chunk cc, once every CTA's partial has landed; -1 on a stuck wait
+    // (flagged; warps 6-7 then stop, and the issuer's bounded wait for them ends the chain)
+    // or once the chain has given up.  Warps 6-7 never write s_abort: the chain reads it
+    // after its own barriers only, where every chain thread must see the same value.
+    auto norm_scale = [&](int cc, int t) {
+        const int bn = cc & 1;
+        if (!mbar_wait_cluster(&s_nb[bn], (uint32_t)((cc >> 1) & 1), &s_abort)) {
+            if (!s_abort) flag_device_error(&g_chunk_error, 7);
+            return -1.f;
+        }
+        float tot = 0.f;
+        for (int q = 0; q < nsl; ++q) tot += s_np[bn][q][t];
+        return rsqrtf(fmaf(tot, 1.f / (float)g.dv, a.norm.eps));
+    };
+    auto norm_store = [&](int cc, int t, float rinv) {  // normalise and store row t of chunk cc (in o_prev)
+        const int t0 = tb + cc * kC, cnt = min(kC, te - t0);
+        if (rinv >= 0.f && t < cnt) {
+            const size_t at = ((size_t)(t0 + t) * g.Hv + h) * g.dv + col0;
+            float zv[kNS], yv[kNS];
+            unpack_row32<T>(z_raw, zv);
+            silu_fast_n(zv, yv);
+#pragma unroll
+            for (int j = 0; j < kNS; ++j) yv[j] = __fmul_rn(__fmul_rn(s_nw[j], __fmul_rn(o_prev[j], rinv)), yv[j]);
+            store_row32<T>(static_cast<T*>(a.norm.y) + at, yv);
+        }
+    };
     // O rows of chunk cc, by warps 2-3 (rows past the chunk's last token are not stored)
     auto out_rows = [&](int cc) {
         wait_all(&s_o, (uint32_t)(cc & 1));
@@ -845,7 +951,54 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             for (int j = 0; j < kNS; j += 4) st_stream(orow + j, make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]));
         }
     };
+    // NORM: the output rows of every chunk, by warps 6-7 (TMEM lanes 64-127, as warps 2-3)
+    auto norm_rows = [&]() {
+        const int t = 32 * (warp - 6) + lane;
+        const uint32_t wn = (uint32_t)(32 * (warp & 3)) << 16;
+        for (int cc = 0; cc < nch; ++cc) {
+            const int b = cc & 1;
+            if (!mbar_wait_or_abort(&s_on[b], (uint32_t)((cc >> 1) & 1), &s_abort)) {
+                if (!s_abort) flag_device_error(&g_chunk_error, 7);
+                return;
+            }
+            umma::fence_after_sync();
+            float ov[kNS];
+            tmem_pair(tA0 + 64 * b + wn, ov);
+            umma::fence_before_sync();
+            mbar_arrive(&s_oc[b]);  // tA[b] is free for round A of chunk cc + 2
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < kNS; ++j) ss = fmaf(ov[j], ov[j], ss);
+            const float rinv = prev_c >= 0 ? norm_scale(prev_c, t) : 0.f;
+            if (rinv < 0.f) return;
+            if (t == 0) mbar_arrive_expect_tx(&s_nb[b], (uint32_t)(4 * kC * nsl));
+            for (int q = 0; q < nsl; ++q)
+                st_async_cluster(cluster_addr(&s_np[b][crank][t], q), ss, cluster_addr(&s_nb[b], q));
+            if (prev_c >= 0) norm_store(prev_c, t, rinv);
+#pragma unroll
+            for (int j = 0; j < kNS; ++j) o_prev[j] = ov[j];
+            prev_c = cc;
+            const int t0 = tb + cc * kC, cnt = min(kC, te - t0);
+            if (t < cnt) {  // used a chunk later
+                const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const T*>(a.norm.z) +
+                                                                 ((size_t)(t0 + t) * g.Hv + h) * g.dv + col0);
+#pragma unroll
+                for (int q = 0; q < (int)(kNS * sizeof(T) / 16); ++q) z_raw[q] = zp[q];
+            }
+        }
+        if (!s_abort) norm_store(nch - 1, t, norm_scale(nch - 1, t));
+    };
+    // the chain's own barrier (warps 0-4; warps 5-7 of a NORM CTA do not take part)
+    auto chain_sync = [&]() {
+        if (NORM)
+            named_sync(1, kCT);
+        else
+            __syncthreads();
+    };
 
+    if (NORM && warp >= kCT / 32) {
+        if (warp >= 6) norm_rows();
+    } else {
     if (tid == kCopier) {
         load_wq(0);
         if (nch > 1) load_wq(1);
@@ -859,13 +1012,20 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         // ---- round A: [W; Q~] S0 ----
         wait_all(&s_wq[b], (uint32_t)((c >> 1) & 1));
         if (tid == kIssuer) {
+            if (NORM && c >= 2) {  // warps 6-7 have read O of chunk c - 2 out of tA[b]
+                if (!mbar_wait_or_abort(&s_oc[b], (uint32_t)(((c - 2) >> 1) & 1), &s_abort)) s_abort = 1;
+                umma::fence_after_sync();
+            }
             umma::mma_split_bpair(tA0 + 64 * b, wqb + b * kWQBytes, false, s0t, 2 * kC, kNS, kDK, false);
             umma::commit(&s_a);
             ++a_iss;
         }
         if (warp == 2 || warp == 3) {
             if (c > 0) {
-                out_rows(c - 1);
+                if (!NORM)
+                    out_rows(c - 1);
+                else if (tid == kCopier)
+                    wait_all(&s_o, (uint32_t)((c - 1) & 1));
                 if (tid == kCopier) load_p(c);  // P U of chunk c-1 has completed: the P buffer is free
             }
         } else if (warp < 2) {  // U = u - X, rows 0-63
@@ -889,7 +1049,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         }
         fence_proxy_async_smem();
         umma::fence_before_sync();
-        __syncthreads();
+        chain_sync();
         if (s_abort) break;
         umma::fence_after_sync();
 
@@ -902,6 +1062,7 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
             if (!mbar_wait_bounded(&s_p, (uint32_t)(c & 1))) s_abort = 1;
             umma::mma_split_bpair(tA0 + 64 * b, pp, false, ut, 2 * kC, kNS, kC, true);
             umma::commit(&s_o);
+            if (NORM) umma::commit(&s_on[b]);
             ++b_iss;
         }
         if (srow) {
@@ -920,11 +1081,12 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
         }
         fence_proxy_async_smem();
         umma::fence_before_sync();
-        __syncthreads();
+        chain_sync();
         if (s_abort) break;
         umma::fence_after_sync();
     }
-    if (!s_abort && (warp == 2 || warp == 3)) out_rows(nch - 1);
+    if (!NORM && !s_abort && (warp == 2 || warp == 3)) out_rows(nch - 1);
+    }
     // on abort, let copies and MMAs still in flight land before TMEM and shared memory
     // are released: wait for the last issued phase of each barrier (a completed phase
     // returns at once)
@@ -946,6 +1108,10 @@ __global__ void __launch_bounds__(kCT, 1) chain_kernel(const PrefillArgs a, cons
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_free(tmem, 256);
+    if (NORM) {  // no CTA leaves while a peer may still write into its shared memory
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    }
     if (s_abort || !srow) return;
 #pragma unroll
     for (int j = 0; j < kNS; j += 4) *reinterpret_cast<float4*>(Sg + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -1010,10 +1176,29 @@ cudaError_t launch_chunked_t(const PrefillArgs& a, const GateParams& gp, int nch
     chunk_prep_kernel<T><<<std::min(nitems, sms), kPT, prep_smem, stream>>>(a, coff, out, gp, nchunk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
+    const dim3 grid(g.dv / kNS, g.Hv, a.N);
+    if (!a.norm.z) {
+        e = cudaFuncSetAttribute(chain_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
+        if (e != cudaSuccess) return e;
+        chain_kernel<T, false><<<grid, kCT, kChainSmem, stream>>>(a, coff, out);
+        return cudaGetLastError();
+    }
+    // the gated RMSNorm fused: the dv/32 CTAs of a value head form one cluster
+    e = cudaFuncSetAttribute(chain_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
     if (e != cudaSuccess) return e;
-    chain_kernel<T><<<dim3(g.dv / kNS, g.Hv, a.N), kCT, kChainSmem, stream>>>(a, coff, out);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kCTN);
+    cfg.dynamicSmemBytes = kChainSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = g.dv / kNS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chain_kernel<T, true>, a, coff, out);
 }
 }  // namespace
 

@@ -46,6 +46,22 @@ __device__ __forceinline__ float4 ld_stream(const float* p) { return __ldcs(rein
 __device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
 __device__ __forceinline__ float silu(float y) { return y / (1.f + expf(-y)); }
+// SiLU from the fast exponential and division intrinsics, for the output gate of the
+// prefill's fused norm, where it is one factor of a product that is then rounded to
+// the io type: relative error about 1e-6 for |y| < 10 (the exact form's IEEE division
+// costs several times the instructions).  Below y = -87 the denominator passes 2^126
+// and __fdividef gives 0, where silu(y) is under 1e-35.
+__device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.f + __expf(-y)); }
+// silu_fast of N values as separate passes (the exponentials, then the quotients), so
+// the N special-function chains overlap; written as one loop of silu_fast calls they
+// were compiled to run one after another, at several times the cost.
+template <int N>
+__device__ __forceinline__ void silu_fast_n(const float (&y)[N], float (&s)[N]) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) s[j] = __expf(-y[j]);
+#pragma unroll
+    for (int j = 0; j < N; ++j) s[j] = __fdividef(y[j], 1.f + s[j]);
+}
 
 // Gate parameterisation of section 1.2: with per-value-head A_log and dt_bias
 // set, the gate input is the raw projection a and the log-decay is

@@ -93,11 +93,17 @@ struct PrefillArgs {
     float* out;                // [T, Hv, dv]
     void* ws;                  // workspace
     size_t ws_bytes;
+    NormParams norm;           // z set: the gated RMSNorm fused, y written instead of out
 };
 size_t prefill_resident_workspace(const Geom& g, int N, long long T);
 cudaError_t launch_prefill_resident(const PrefillArgs& a, const GateParams& gp, cudaStream_t stream);
 // Steps 1-4 for every packed token into token-major normalised fp32 rows y [T, D].
 cudaError_t launch_prefill_prep(const PrefillArgs& a, float* y, cudaStream_t stream);
+
+// The gated RMSNorm fused into a prefill form's output epilogue: the CTAs that hold
+// one head's columns form a cluster and exchange the rows' sums of squares.
+bool prefill_norm_supported(const Geom& g, int variant);
+cudaError_t prefill_error_read(int32_t* value, bool clear);
 
 // Chunked (tensor-core) prefill, gdn_chunked.cu.
 bool prefill_chunked_supported(const Geom& g);

@@ -15,12 +15,18 @@
 //          below).  It also writes each sequence's new conv state: the prep
 //          launch has finished reading the old one by then.
 // The resident form stays serial in the sequence length, 8 tokens at a time.
+// With the gated RMSNorm fused (section 2), the dv/16 block CTAs of a value head
+// form a cluster and exchange the rows' sums of squares (see block_kernel).
 #include <algorithm>
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tma.cuh"
 
 namespace gdn {
+
+static __device__ int32_t g_prefill_error;  // set to GDN_ERR_DEVICE_TIMEOUT (7) by a stuck wait
+
 namespace {
 
 constexpr int kPrepTokens = 32;
@@ -237,7 +243,17 @@ struct BlockCfg {
     __device__ __forceinline__ static int at(int row) { return row + (row / RPL) * 4; }
 };
 
-template <typename T, int DK>
+// NORM: the output rows get the gated RMSNorm, which needs each row's sum of squares
+// over all dv columns: the dv/16 CTAs of a value head form a cluster; after a block,
+// each CTA sends its rows' partial sums (over its 16 columns) to every CTA of the
+// cluster (asynchronous stores into their shared memory that complete bytes on their
+// barriers).  The exchange rides on the block's first barrier: at block e, after it,
+// each CTA reads the sums of block e-2, sends its partials of block e-1 (written to
+// s_wss before the previous block's last barrier), then normalises and stores block
+// e-2, whose raw outputs and z values wait in registers.  A peer's buffer is thus
+// rewritten only after its reads of the buffer's previous use (they precede the send
+// this CTA waited for), and the partials have a whole block to arrive.
+template <typename T, int DK, bool NORM>
 __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const GateParams gp, const float* __restrict__ y,
                                                     const float* __restrict__ gram) {
     using R = BlockCfg<DK>;
@@ -249,6 +265,10 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
     __shared__ float s_gram[kBM][16];
     __shared__ float s_g[kBM], s_b[kBM], s_gam[kBM], s_c[kBM];
     __shared__ __align__(16) float s_Gkk[kBM][kBM], s_Gkq[kBM][kBM];
+    // NORM: per-warp partial sums of the block's rows, and the cluster's partials by block parity
+    __shared__ float s_wss[kBW][kBM];
+    __shared__ float s_np[NORM ? 2 : 1][NORM ? 8 : 1][kBM];
+    __shared__ __align__(8) uint64_t s_nb[2];
     const Geom& g = a.g;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hk = h / g.f, col0 = slice * kBC;
@@ -275,6 +295,58 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
             }
     }
     if (len <= 0) return;
+    const int ncta = g.dv / kBC;  // CTAs of the cluster (NORM)
+    if (NORM) {
+        if (tid == 0) {
+            mbar_init(&s_nb[0], 1);  // one local arrive.expect_tx; the bytes come from the whole cluster
+            mbar_init(&s_nb[1], 1);
+            fence_mbar_init();
+        }
+        cluster_arrive_release();  // every CTA's barriers exist before any remote arrive
+        cluster_wait_acquire();
+    }
+    const uint32_t crank = NORM ? cluster_ctarank() : 0;
+    // the raw outputs of the last two blocks this thread holds (1: the block before, 2: the
+    // one before that), their z values (io type, converted at use so that no thread waits
+    // on the load) and token ranges, and the norm weight of its column
+    float o1 = 0.f, o2 = 0.f;
+    T z1 = T(), z2 = T();
+    int t01 = 0, cnt1 = 0, t02 = 0, cnt2 = 0, e = 0;
+    const float w_col = NORM ? a.norm.weight[col0 + col] : 0.f;
+    // 1/RMS of row rl of block pe, once every CTA's partial has landed (-1 on a stuck wait)
+    auto norm_scale = [&](int pe) {
+        const int bn = pe & 1;
+        if (!mbar_wait_cluster(&s_nb[bn], (uint32_t)((pe >> 1) & 1), nullptr)) {
+            flag_device_error(&g_prefill_error, 7);
+            return -1.f;
+        }
+        float tot = 0.f;
+        for (int q = 0; q < ncta; ++q) tot += s_np[bn][q][rl];
+        return rsqrtf(fmaf(tot, 1.f / (float)g.dv, a.norm.eps));
+    };
+    auto norm_store = [&](int pt0, int pcnt, float o, T z, float rinv) {
+        if (rinv >= 0.f && rl < pcnt) {
+            const size_t at = ((size_t)(pt0 + rl) * g.Hv + h) * g.dv + col0 + col;
+            static_cast<T*>(a.norm.y)[at] =
+                from_f32<T>(__fmul_rn(__fmul_rn(w_col, __fmul_rn(o, rinv)), silu_fast(to_f32(z))));
+        }
+    };
+    // this CTA's partial sums of block pe's rows (in s_wss) to every CTA of the cluster
+    auto norm_send = [&](int pe) {
+        if (tid < kBM) {
+            const float p = (s_wss[0][tid] + s_wss[1][tid]) + (s_wss[2][tid] + s_wss[3][tid]);
+            const int bn = pe & 1;
+            if (tid == 0) mbar_arrive_expect_tx(&s_nb[bn], (uint32_t)(4 * kBM * ncta));
+            for (int q = 0; q < ncta; ++q)
+                st_async_cluster(cluster_addr(&s_np[bn][crank][tid], q), p, cluster_addr(&s_nb[bn], q));
+        }
+    };
+    // at block e (or after the last block, e = the block count): blocks e-2 and e-1
+    auto norm_step = [&]() {
+        const float r2 = e >= 2 ? norm_scale(e - 2) : -1.f;
+        norm_send(e - 1);
+        if (e >= 2) norm_store(t02, cnt2, o2, z2, r2);
+    };
 
     float S[RPL];
 #pragma unroll
@@ -325,6 +397,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
         if (tid < kBM * 16) s_gram[tid >> 4][tid & 15] = pgr;
         __syncthreads();
         if (t0 + kBM < te) fetch(t0 + kBM);  // next block's loads fly under this block
+        if (NORM && e >= 1) norm_step();
 
         // ---- block coefficients (warp 0) ----
         if (warp == 0) {
@@ -401,7 +474,20 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
             for (int s2 = 0; s2 <= t; ++s2) o = fmaf(s_Gkq[t][s2], dl[s2], o);
             if (t == rl) o_mine = o;
         }
-        if (rl < cnt) a.out[((size_t)(t0 + rl) * g.Hv + h) * g.dv + col0 + col] = o_mine;
+        if (NORM) {
+            // this CTA's partial of row rl: the warp's 4 columns (lanes rl + 8 cw), then the 4 warps
+            // (summed and sent at the next block, after its first barrier)
+            float ss = __fmul_rn(o_mine, o_mine);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+            if (cw == 0) s_wss[warp][rl] = ss;
+            o2 = o1, z2 = z1, t02 = t01, cnt2 = cnt1;
+            o1 = o_mine, t01 = t0, cnt1 = cnt;
+            if (rl < cnt) z1 = static_cast<const T*>(a.norm.z)[((size_t)(t0 + rl) * g.Hv + h) * g.dv + col0 + col];
+            ++e;
+        } else if (rl < cnt) {
+            a.out[((size_t)(t0 + rl) * g.Hv + h) * g.dv + col0 + col] = o_mine;
+        }
 
         // ---- S <- gamma_last S + sum_s c_s k_s delta_s^T ----
         const float gl = s_gam[kBM - 1];
@@ -419,6 +505,12 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
             S[4 * r4 + 0] = x0; S[4 * r4 + 1] = x1; S[4 * r4 + 2] = x2; S[4 * r4 + 3] = x3;
         }
         __syncthreads();  // the block's shared data is consumed
+    }
+    if (NORM) {
+        norm_step();  // the last block's partials are in s_wss (the loop's last barrier)
+        norm_store(t01, cnt1, o1, z1, norm_scale(e - 1));
+        cluster_arrive_release();  // no CTA leaves while a peer may still write into its shared memory
+        cluster_wait_acquire();
     }
 #pragma unroll
     for (int r = 0; r < RPL; ++r) Sg[(size_t)(rl * RPL + r) * g.dv] = S[r];
@@ -448,8 +540,26 @@ cudaError_t launch_resident_t(const PrefillArgs& a, const GateParams& gp, cudaSt
     gram_kernel<DK><<<dim3((a.T + kGramTok - 1) / kGramTok, g.Hk), 256, gram_smem, stream>>>(a, y, gram);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    block_kernel<T, DK><<<dim3(g.dv / BlockCfg<DK>::BC, g.Hv, a.N), kBT, 0, stream>>>(a, gp, y, gram);
-    return cudaGetLastError();
+    const dim3 grid(g.dv / BlockCfg<DK>::BC, g.Hv, a.N);
+    if (!a.norm.z) {
+        block_kernel<T, DK, false><<<grid, kBT, 0, stream>>>(a, gp, y, gram);
+        return cudaGetLastError();
+    }
+    // the gated RMSNorm fused: the dv/16 CTAs of a value head form one cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, block_kernel<T, DK, true>, a, gp, static_cast<const float*>(y),
+                              static_cast<const float*>(gram));
 }
 
 }  // namespace
@@ -460,6 +570,20 @@ cudaError_t launch_prefill_prep(const PrefillArgs& a, float* y, cudaStream_t s) 
 
 size_t prefill_resident_workspace(const Geom& g, int /*N*/, long long T) {
     return (size_t)T * g.D * sizeof(float) + (size_t)T * g.Hk * 16 * sizeof(float);
+}
+
+// Fused norm: one cluster per value head, dv/16 CTAs (resident) or dv/32 (chunked),
+// at most the portable cluster size of 8.
+bool prefill_norm_supported(const Geom& g, int variant) {
+    if (variant == 0) return g.dv / 16 <= 8;
+    return prefill_chunked_supported(g);
+}
+
+cudaError_t prefill_error_read(int32_t* value, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_prefill_error, sizeof(int32_t));
+    if (e != cudaSuccess || !clear) return e;
+    const int32_t zero = 0;
+    return cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(int32_t));
 }
 
 cudaError_t launch_prefill_resident(const PrefillArgs& a, const GateParams& gp, cudaStream_t s) {

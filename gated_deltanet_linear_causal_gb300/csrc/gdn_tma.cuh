@@ -89,6 +89,39 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
     return false;
 }
 
+// ---- distributed shared memory (thread-block clusters) ----------------------
+// The address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+// Asynchronous store of v into the shared memory of a cluster CTA (addr from
+// cluster_addr) that completes its 4 bytes as transaction bytes on that CTA's mbarrier
+// (bar_addr, likewise mapped): the receiver's phase completes once its own
+// arrive.expect_tx and all the bytes it expects have landed.
+__device__ __forceinline__ void st_async_cluster(uint32_t addr, float v, uint32_t bar_addr) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];\n" ::"r"(addr), "f"(v),
+                 "r"(bar_addr)
+                 : "memory");
+}
+// Wait (acquire at cluster scope) for phase `parity` of a local mbarrier that other
+// CTAs of the cluster arrive on; false after kWaitLimit polls or once *abort is set.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (abort && *abort) return false;
+    }
+    return false;
+}
+
 // Arrive on named barrier `id` without waiting (the barrier completes when `count`
 // threads have arrived or synced on it).
 __device__ __forceinline__ void named_arrive(int id, int count) {

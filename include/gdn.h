@@ -166,6 +166,31 @@ gdn_status_t gdn_forward_prefill(const gdn_config_t *cfg, int32_t num_seqs,
                                  size_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * Prefill with the gated RMSNorm of section 2 ("Gated RMSNorm": the linear
+ * attention layer applies attn_out = norm(attn_out, z) right after the
+ * recurrence) fused into the output epilogue: as gdn_forward_prefill, but instead
+ * of the fp32 output it writes
+ *   y    device [T, Hv, dv] io dtype, gdn_gated_rmsnorm of the call's output
+ * from z (device [T, Hv, dv] io dtype), norm_weight (device [dv] fp32) and
+ * norm_eps.  z, y and norm_weight are 16-byte aligned; y must not overlap the
+ * other buffers.  The CTAs that hold one value head's columns form a thread-block
+ * cluster and exchange the rows' sums of squares, so the row is normalised without
+ * writing the fp32 output to memory.  Both variants; head_v_dim <= 128
+ * (GDN_ERR_UNSUPPORTED otherwise: call gdn_forward_prefill, then
+ * gdn_gated_rmsnorm).  Workspace, states, sizes and errors as gdn_forward_prefill.
+ */
+gdn_status_t gdn_forward_prefill_gated(const gdn_config_t *cfg, int32_t num_seqs,
+                                       const int32_t *cu_seqlens,
+                                       const int32_t *cu_seqlens_host,
+                                       const void *qkv, const void *conv_weight,
+                                       const float *gate, const float *beta,
+                                       void *conv_state, float *ssm_state,
+                                       const void *z, const float *norm_weight,
+                                       float norm_eps, void *y, int32_t variant,
+                                       void *workspace, size_t workspace_bytes,
+                                       gdn_stream_t stream);
+
+/*
  * Prefill for callers that cannot allocate device memory.  (The pages have no
  * counterpart: this is a deployment convenience, not part of the layer.)
  *
