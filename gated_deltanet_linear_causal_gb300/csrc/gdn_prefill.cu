@@ -247,12 +247,14 @@ struct BlockCfg {
 // over all dv columns: the dv/16 CTAs of a value head form a cluster; after a block,
 // each CTA sends its rows' partial sums (over its 16 columns) to every CTA of the
 // cluster (asynchronous stores into their shared memory that complete bytes on their
-// barriers).  The exchange rides on the block's first barrier: at block e, after it,
-// each CTA reads the sums of block e-2, sends its partials of block e-1 (written to
-// s_wss before the previous block's last barrier), then normalises and stores block
-// e-2, whose raw outputs and z values wait in registers.  A peer's buffer is thus
-// rewritten only after its reads of the buffer's previous use (they precede the send
-// this CTA waited for), and the partials have a whole block to arrive.
+// barriers).  The exchange rides on the block's own barriers: at block e, warp 3
+// waits for the partials of block e-2 after the first barrier (while warp 0 computes
+// the block's coefficients), every thread reads their sums after the second (the
+// barrier makes them visible), and after the third the CTA sends its partials of
+// block e-1 and normalises and stores block e-2, whose raw outputs and z values wait
+// in registers.  A peer's buffer is thus rewritten only after its reads of the
+// buffer's previous use (they precede the send this CTA waited for), and the
+// partials have a whole block to arrive.
 template <typename T, int DK, bool NORM>
 __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const GateParams gp, const float* __restrict__ y,
                                                     const float* __restrict__ gram) {
@@ -266,9 +268,10 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
     __shared__ float s_g[kBM], s_b[kBM], s_gam[kBM], s_c[kBM];
     __shared__ __align__(16) float s_Gkk[kBM][kBM], s_Gkq[kBM][kBM];
     // NORM: per-warp partial sums of the block's rows, and the cluster's partials by block parity
-    __shared__ float s_wss[kBW][kBM];
+    __shared__ float s_wss[2][kBW][kBM];  // by block parity
     __shared__ float s_np[NORM ? 2 : 1][NORM ? 8 : 1][kBM];
     __shared__ __align__(8) uint64_t s_nb[2];
+    __shared__ int s_nfail;  // NORM: a wait for the partials gave up (read after barriers only)
     const Geom& g = a.g;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int hk = h / g.f, col0 = slice * kBC;
@@ -298,6 +301,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
     const int ncta = g.dv / kBC;  // CTAs of the cluster (NORM)
     if (NORM) {
         if (tid == 0) {
+            s_nfail = 0;
             mbar_init(&s_nb[0], 1);  // one local arrive.expect_tx; the bytes come from the whole cluster
             mbar_init(&s_nb[1], 1);
             fence_mbar_init();
@@ -313,13 +317,18 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
     T z1 = T(), z2 = T();
     int t01 = 0, cnt1 = 0, t02 = 0, cnt2 = 0, e = 0;
     const float w_col = NORM ? a.norm.weight[col0 + col] : 0.f;
-    // 1/RMS of row rl of block pe, once every CTA's partial has landed (-1 on a stuck wait)
+    // warp 3: wait until every CTA's partials of block pe have landed (gives up for good,
+    // flagged, on a stuck wait)
+    auto norm_wait = [&](int pe) {
+        if (!s_nfail && !mbar_wait_cluster(&s_nb[pe & 1], (uint32_t)((pe >> 1) & 1), nullptr)) {
+            flag_device_error(&g_prefill_error, 7);
+            s_nfail = 1;
+        }
+    };
+    // 1/RMS of row rl of block pe, after a barrier that follows norm_wait(pe); -1 after a failed wait
     auto norm_scale = [&](int pe) {
         const int bn = pe & 1;
-        if (!mbar_wait_cluster(&s_nb[bn], (uint32_t)((pe >> 1) & 1), nullptr)) {
-            flag_device_error(&g_prefill_error, 7);
-            return -1.f;
-        }
+        if (s_nfail) return -1.f;
         float tot = 0.f;
         for (int q = 0; q < ncta; ++q) tot += s_np[bn][q][rl];
         return rsqrtf(fmaf(tot, 1.f / (float)g.dv, a.norm.eps));
@@ -334,18 +343,12 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
     // this CTA's partial sums of block pe's rows (in s_wss) to every CTA of the cluster
     auto norm_send = [&](int pe) {
         if (tid < kBM) {
-            const float p = (s_wss[0][tid] + s_wss[1][tid]) + (s_wss[2][tid] + s_wss[3][tid]);
             const int bn = pe & 1;
+            const float p = (s_wss[bn][0][tid] + s_wss[bn][1][tid]) + (s_wss[bn][2][tid] + s_wss[bn][3][tid]);
             if (tid == 0) mbar_arrive_expect_tx(&s_nb[bn], (uint32_t)(4 * kBM * ncta));
             for (int q = 0; q < ncta; ++q)
                 st_async_cluster(cluster_addr(&s_np[bn][crank][tid], q), p, cluster_addr(&s_nb[bn], q));
         }
-    };
-    // at block e (or after the last block, e = the block count): blocks e-2 and e-1
-    auto norm_step = [&]() {
-        const float r2 = e >= 2 ? norm_scale(e - 2) : -1.f;
-        norm_send(e - 1);
-        if (e >= 2) norm_store(t02, cnt2, o2, z2, r2);
     };
 
     float S[RPL];
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
         if (tid < kBM * 16) s_gram[tid >> 4][tid & 15] = pgr;
         __syncthreads();
         if (t0 + kBM < te) fetch(t0 + kBM);  // next block's loads fly under this block
-        if (NORM && e >= 1) norm_step();
+        if (NORM && e >= 2 && warp == 3) norm_wait(e - 2);
 
         // ---- block coefficients (warp 0) ----
         if (warp == 0) {
@@ -423,6 +426,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
             }
         }
         __syncthreads();
+        if (NORM && e >= 2) norm_store(t02, cnt2, o2, z2, norm_scale(e - 2));  // warp 3 waited before the barrier
         for (int idx = tid; idx < kBM * (DK / 4); idx += kBT) {
             const int s2 = idx / (DK / 4), c4 = idx - s2 * (DK / 4);
             const int at = R::at(4 * c4);
@@ -459,6 +463,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
             }
         }
         __syncthreads();  // s_kt, s_Gkk, s_Gkq are ready
+        if (NORM && e >= 1) norm_send(e - 1);  // every thread has read block e-2's sums
 
         // ---- resolve the block's deltas and outputs for this lane's column ----
         float dl[kBM];
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
             float ss = __fmul_rn(o_mine, o_mine);
             ss += __shfl_xor_sync(0xffffffffu, ss, 8);
             ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-            if (cw == 0) s_wss[warp][rl] = ss;
+            if (cw == 0) s_wss[e & 1][warp][rl] = ss;
             o2 = o1, z2 = z1, t02 = t01, cnt2 = cnt1;
             o1 = o_mine, t01 = t0, cnt1 = cnt;
             if (rl < cnt) z1 = static_cast<const T*>(a.norm.z)[((size_t)(t0 + rl) * g.Hv + h) * g.dv + col0 + col];
@@ -506,8 +511,14 @@ __global__ void __launch_bounds__(kBT) block_kernel(const PrefillArgs a, const G
         }
         __syncthreads();  // the block's shared data is consumed
     }
-    if (NORM) {
-        norm_step();  // the last block's partials are in s_wss (the loop's last barrier)
+    if (NORM) {  // blocks e-2 and e-1 (e = the block count); the last block's partials are in s_wss
+        if (e >= 2 && warp == 3) norm_wait(e - 2);
+        __syncthreads();
+        if (e >= 2) norm_store(t02, cnt2, o2, z2, norm_scale(e - 2));
+        __syncthreads();
+        norm_send(e - 1);
+        if (warp == 3) norm_wait(e - 1);
+        __syncthreads();
         norm_store(t01, cnt1, o1, z1, norm_scale(e - 1));
         cluster_arrive_release();  // no CTA leaves while a peer may still write into its shared memory
         cluster_wait_acquire();
