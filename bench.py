@@ -604,6 +604,10 @@ def oracle_decode_rate(steps, state, budget_s, max_steps):
 
 # ---------------------------------------------------------------------------
 
+SECONDARIES = ("prefill_chunked", "prefill_resident", "prefill_gated_norm", "decode_raw_gates", "decode_gated_norm",
+               "verify")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -614,7 +618,11 @@ def main():
     ap.add_argument("--no-secondary", action="store_true", help="headline decode only")
     ap.add_argument("--soak", type=int, default=500, help="untimed decode launches before the timed region")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--only", default="", help="comma list of secondaries to run (default all): " + ", ".join(SECONDARIES))
     args = ap.parse_args()
+    bad = [n for n in args.only.split(",") if n and n not in SECONDARIES]
+    if bad:
+        ap.error(f"unknown secondaries {bad}; choose from {SECONDARIES}")
     args.warmup = max(args.warmup, 3)
 
     if args.impl == "reference":
@@ -636,10 +644,13 @@ def main():
     clocks.start()
     dec = run_decode(args, dev, dist, rank, world, st, steps)
     sec = {}
+    only = set(n for n in args.only.split(",") if n) or set(SECONDARIES)
     if secondary and rank == 0:
         shape = synth.PRODUCTION
         chunk_sources = ["gdn_chunked.cu", "gdn_common.cuh", "gdn_tma.cuh", "gdn_umma.cuh"]
         for name, variant in (("chunked", gb.GDN_PREFILL_CHUNKED), ("resident", gb.GDN_PREFILL_RESIDENT)):
+            if "prefill_" + name not in only:
+                continue
             key = "" if name == "chunked" else "_resident"
             for label, x, rand in (("prefill_L8192", x_long, False), ("prefill_varlen16", x_var, True)):
                 med, times = run_prefill(dev, x, variant)
@@ -661,30 +672,37 @@ def main():
                 else:
                     e["roofline_frac"] = e["hbm_frac"]  # bound by its serial chain; reported against HBM
                 sec[label + key] = e
-        (mf, tf), (mu, _) = run_prefill_gated(dev, x_long, gb.GDN_PREFILL_CHUNKED)
-        sec["prefill_L8192_gated_norm"] = {"variant": "chunked", "tokens_per_s": round(8192 / (mf / 1e3), 1),
-                                           "ms": round(mf, 4), "reps": len(tf), "spread": _spread(tf),
-                                           "ms_prefill_then_norm_kernel": round(mu, 4), "cold_l2": True,
-                                           "note": "gated RMSNorm fused into the chain's output epilogue: bf16 z in, "
-                                                   "bf16 y out, no fp32 output written"}
-        ms = run_decode_raw_gates(dev, st, steps)
-        nb = decode_bytes(shape, B_DECODE) + 2 * 32 * 4
-        sec["decode_B64_raw_gates"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),
-                                       "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                       "algorithmic_bytes": nb,
-                                       "note": "gate = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) in the kernel"}
-        ms, ms_unfused = run_decode_gated(dev, st, steps)
-        nb = decode_bytes(shape, B_DECODE) - B_DECODE * 32 * 128 * 4 + 2 * B_DECODE * 32 * 128 * 2 + 128 * 4
-        sec["decode_B64_gated_norm"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),
-                                        "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                        "algorithmic_bytes": nb, "ms_decode_then_norm_kernel": round(ms_unfused, 5),
-                                        "note": "gated RMSNorm fused: bf16 z in, bf16 y out"}
-        mv, mc, tv = run_verify(dev, x_ver)
-        nb = verify_bytes(shape, 32, 4)
-        sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4), "reps": len(tv),
-                                "spread": _spread(tv),
-                                "roofline_frac": round(nb / (mv / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                                "algorithmic_bytes": nb, "commit_ms": round(mc, 4), "cold_l2": True}
+        for name, variant in (("chunked", gb.GDN_PREFILL_CHUNKED), ("resident", gb.GDN_PREFILL_RESIDENT)):
+            if "prefill_gated_norm" not in only:
+                break
+            (mf, tf), (mu, _) = run_prefill_gated(dev, x_long, variant)
+            key = "" if name == "chunked" else "_resident"
+            sec["prefill_L8192_gated_norm" + key] = {
+                "variant": name, "tokens_per_s": round(8192 / (mf / 1e3), 1), "ms": round(mf, 4), "reps": len(tf),
+                "spread": _spread(tf), "ms_prefill_then_norm_kernel": round(mu, 4), "cold_l2": True,
+                "note": "gated RMSNorm fused into the output epilogue (clusters exchange the rows' sums of squares): "
+                        "bf16 z in, bf16 y out, no fp32 output written"}
+        if "decode_raw_gates" in only:
+            ms = run_decode_raw_gates(dev, st, steps)
+            nb = decode_bytes(shape, B_DECODE) + 2 * 32 * 4
+            sec["decode_B64_raw_gates"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),
+                                           "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                           "algorithmic_bytes": nb,
+                                           "note": "gate = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) in the kernel"}
+        if "decode_gated_norm" in only:
+            ms, ms_unfused = run_decode_gated(dev, st, steps)
+            nb = decode_bytes(shape, B_DECODE) - B_DECODE * 32 * 128 * 4 + 2 * B_DECODE * 32 * 128 * 2 + 128 * 4
+            sec["decode_B64_gated_norm"] = {"tokens_per_s": round(B_DECODE / (ms / 1e3), 1), "ms": round(ms, 5),
+                                            "roofline_frac": round(nb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                            "algorithmic_bytes": nb, "ms_decode_then_norm_kernel": round(ms_unfused, 5),
+                                            "note": "gated RMSNorm fused: bf16 z in, bf16 y out"}
+        if "verify" in only:
+            mv, mc, tv = run_verify(dev, x_ver)
+            nb = verify_bytes(shape, 32, 4)
+            sec["verify_B32_L4"] = {"tokens_per_s": round(128 / (mv / 1e3), 1), "ms": round(mv, 4), "reps": len(tv),
+                                    "spread": _spread(tv),
+                                    "roofline_frac": round(nb / (mv / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                                    "algorithmic_bytes": nb, "commit_ms": round(mc, 4), "cold_l2": True}
     clk = clocks.stop()
     if rank != 0:
         if dist:

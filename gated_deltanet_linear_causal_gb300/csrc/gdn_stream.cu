@@ -183,8 +183,13 @@ __device__ __forceinline__ TileRef tile_ref(const Geom& g, int item, int r, bool
 // l with l % 8 == w, spreading the gate arithmetic over the eight warps.  `at` is
 // the row's first element index, zrow the row's z, copied into shared memory by
 // the producer with the item's first state tile.
+// Gated RMSNorm of one output row (o: this lane's 4 columns, the same in every compute
+// warp; w4: the norm weights of those columns): the row's sum of squares by warp
+// shuffles, then each warp stores the columns of the lanes l with l % 8 == warp.  The
+// SiLU of the gate is the fast-intrinsic form: it is one factor of a product rounded
+// to the io type.
 template <typename T>
-__device__ __forceinline__ void norm_out(const NormParams& np, size_t at, float4 o, int dv, const T* zrow) {
+__device__ __forceinline__ void norm_out(const NormParams& np, size_t at, float4 o, int dv, const T* zrow, float4 w4) {
     const int lane = threadIdx.x & 31, c = 4 * lane;
     float ss = __fmul_rn(o.x, o.x);
     ss = fmaf(o.y, o.y, ss);
@@ -194,15 +199,15 @@ __device__ __forceinline__ void norm_out(const NormParams& np, size_t at, float4
     for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rinv = rsqrtf(fmaf(ss, 1.f / (float)dv, np.eps));
     if ((lane & (kComputeWarps - 1)) != (int)(threadIdx.x >> 5)) return;
-    const float4 w4 = __ldg(reinterpret_cast<const float4*>(np.weight + c));
     T* yr = static_cast<T*>(np.y) + at + c;
     const float ov[4] = {o.x, o.y, o.z, o.w}, wv[4] = {w4.x, w4.y, w4.z, w4.w};
-    float zv[4];
+    float zv[4], sz[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) zv[e] = to_f32(zrow[c + e]);
+    silu_fast_n(zv, sz);
     T yv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) yv[e] = from_f32<T>(__fmul_rn(__fmul_rn(wv[e], __fmul_rn(ov[e], rinv)), silu(zv[e])));
+    for (int e = 0; e < 4; ++e) yv[e] = from_f32<T>(__fmul_rn(__fmul_rn(wv[e], __fmul_rn(ov[e], rinv)), sz[e]));
 #pragma unroll
     for (int e = 0; e < 4; ++e) yr[e] = yv[e];
 }
@@ -450,6 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
     }
 
     // ---- compute: step 5 on every tile of every item ----
+    // NORM (dv == 128): the norm weights of this lane's 4 columns, for every row
+    const float4 nw4 = NORM ? __ldg(reinterpret_cast<const float4*>(np.weight + 4 * lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
     int ustep = 0;  // running token-step counter: alternates the reduction buffers and snapshot stages
     const bool staged = !IN_PLACE && snap_stage;
     // a snapshot stage, once every warp has written its rows (warps 1-7 arrive on kBarSnap,
@@ -493,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 if (NORM)
                     norm_out<T>(np, gi * g.dv, o, g.dv,
                                 reinterpret_cast<const T*>(zs_buf) + (size_t)(i % (nstage + 1)) * fi * g.dv +
-                                    tr.hl * g.dv);
+                                    tr.hl * g.dv,
+                                nw4);
                 else if (warp == 0) st_stream(a.out + gi * g.dv + tr.col0 + Tile<DK>::col4(), o);
                 if (staged) {
                     float* stg = snap_buf + (size_t)sbuf * DK * kTileCols;
