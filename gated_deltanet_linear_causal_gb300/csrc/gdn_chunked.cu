@@ -151,10 +151,6 @@ struct ChunkOut {
     float* gl;
 };
 
-// SiLU with the fast exponential and reciprocal: the chunked form is checked
-// against the oracle's tolerance, not bit for bit against the decode path.
-__device__ __forceinline__ float silu_fast(float y) { return __fmul_rn(y, __frcp_rn(__fadd_rn(1.f, __expf(-y)))); }
-
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -253,7 +249,9 @@ __device__ __forceinline__ void taps8(const T* wb, int c, int K, float (&w)[8][k
 }
 
 // Depthwise causal conv + SiLU of channels c..c+7 (c % 8 == 0) of buffer rb at
-// chunk token t (positions t .. t+K-1 of the rows, newest last).
+// chunk token t (positions t .. t+K-1 of the rows, newest last).  The SiLU is the
+// fast-intrinsic form (the chunked form is checked against the oracle's tolerance,
+// not bit for bit against the decode path), applied in passes after all the sums.
 template <typename T>
 __device__ __forceinline__ void conv8(const RawBuf<T>& rb, int t, int c, int K, float (&y)[8]) {
     const int4 da = *reinterpret_cast<const int4*>(rb.dcol + c), db = *reinterpret_cast<const int4*>(rb.dcol + c + 4);
@@ -267,8 +265,9 @@ __device__ __forceinline__ void conv8(const RawBuf<T>& rb, int t, int c, int K, 
 #pragma unroll
         for (int tap = 0; tap < kKC; ++tap)
             if (tap < K) acc = fmaf(w[e][tap], to_f32(x[tap]), acc);
-        y[e] = silu_fast(acc);
+        y[e] = acc;
     }
+    silu_fast_n(y, y);
 }
 
 // The same at tokens t and t+1 (positions t .. t+K of the rows): the window is
@@ -292,9 +291,11 @@ __device__ __forceinline__ void conv8x2(const RawBuf<T>& rb, int t, int c, int K
                 a0 = fmaf(w[e][tap], xv[tap], a0);
                 a1 = fmaf(w[e][tap], xv[tap + 1], a1);
             }
-        y0[e] = silu_fast(a0);
-        y1[e] = silu_fast(a1);
+        y0[e] = a0;
+        y1[e] = a1;
     }
+    silu_fast_n(y0, y0);
+    silu_fast_n(y1, y1);
 }
 
 // T = (I + A)^-1 for strictly lower A into Tb (both row stride kAld, 16-byte

@@ -54,13 +54,14 @@ __device__ __forceinline__ float silu(float y) { return y / (1.f + expf(-y)); }
 __device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.f + __expf(-y)); }
 // silu_fast of N values as separate passes (the exponentials, then the quotients), so
 // the N special-function chains overlap; written as one loop of silu_fast calls they
-// were compiled to run one after another, at several times the cost.
+// were compiled to run one after another, at several times the cost.  s may be y.
 template <int N>
 __device__ __forceinline__ void silu_fast_n(const float (&y)[N], float (&s)[N]) {
+    float e[N];
 #pragma unroll
-    for (int j = 0; j < N; ++j) s[j] = __expf(-y[j]);
+    for (int j = 0; j < N; ++j) e[j] = __expf(-y[j]);
 #pragma unroll
-    for (int j = 0; j < N; ++j) s[j] = __fdividef(y[j], 1.f + s[j]);
+    for (int j = 0; j < N; ++j) s[j] = __fdividef(y[j], 1.f + e[j]);
 }
 
 // Gate parameterisation of section 1.2: with per-value-head A_log and dt_bias
