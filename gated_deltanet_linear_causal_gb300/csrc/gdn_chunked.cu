@@ -309,19 +309,29 @@ __device__ __forceinline__ void conv8x2(const RawBuf<T>& rb, int t, int c, int K
 //   of its index.
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-__device__ __forceinline__ void inverse_blocked(const float* A, float* Tb, float* X, int gt, int bar) {
+__device__ __forceinline__ void inverse_blocked(const float* __restrict__ A, float* __restrict__ Tb,
+                                                float* __restrict__ X, int gt, int bar) {
     constexpr int kG = kPT / 2;
     if (gt < kC) {
+        // the three buffers are distinct, so the A loads of later rows may be issued ahead
+        // of this column's stores (they are not held back behind them)
         const int o = 16 * (gt >> 4), u = gt & 15;
         float tc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+            float ar[16];
+#pragma unroll
+            for (int s4 = 0; s4 < i; s4 += 4) {
+                const float4 v = ld4(A + (o + i) * kAld + o + s4);
+                ar[s4] = v.x; ar[s4 + 1] = v.y; ar[s4 + 2] = v.z; ar[s4 + 3] = v.w;
+            }
             float acc = 0.f;
 #pragma unroll
-            for (int s = 0; s < i; ++s) acc = fmaf(A[(o + i) * kAld + o + s], tc[s], acc);
+            for (int s = 0; s < i; ++s) acc = fmaf(ar[s], tc[s], acc);
             tc[i] = i < u ? 0.f : i == u ? 1.f : -acc;
-            Tb[(o + i) * kAld + o + u] = tc[i];
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Tb[(o + i) * kAld + o + u] = tc[i];
 #pragma unroll
         for (int i = 0; i < 16; ++i)  // the rest of the block row right of the diagonal block
             for (int jb = o + 16; jb < kC; jb += 16) Tb[(o + i) * kAld + jb + u] = 0.f;
