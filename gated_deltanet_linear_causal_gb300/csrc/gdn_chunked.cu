@@ -129,8 +129,7 @@ struct PrepSmem {
     static constexpr size_t qimg = kimg + kImgBytes;               // Q image, then each head's V image
     static constexpr size_t timg = qimg + kImgBytes;               // T diag(beta gamma), T diag(beta)
     static constexpr size_t kk = timg + 2 * kPBytes;               // fp32 K K^T [64][65]
-    static constexpr size_t qk = kk + kC * kLd * 4;                // fp32 Q K^T [64][65]
-    static constexpr size_t ab = qk + kC * kLd * 4;                // fp32 A [64][68]
+    static constexpr size_t ab = kk + kC * kLd * 4;                // fp32 A [64][68]
     static constexpr size_t tb = ab + kC * kAld * 4;               // fp32 T [64][68]
     static constexpr size_t raw = tb + kC * kAld * 4;              // RawCfg<T>::bufs raw-input buffers
     static constexpr size_t nrm = raw + RawCfg<T>::bufs * RawCfg<T>::buf_bytes;  // fp32 partial sums of squares [8][64]
@@ -418,7 +417,6 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     unsigned char* qimg = smem + L::qimg;  // the V image of each value head after the Gram products
     unsigned char* timg = smem + L::timg;
     float* kk = reinterpret_cast<float*>(smem + L::kk);
-    float* qk = reinterpret_cast<float*>(smem + L::qk);
     float* Ab = reinterpret_cast<float*>(smem + L::ab);
     float* Tb = reinterpret_cast<float*>(smem + L::tb);
     using R = RawCfg<T>;
@@ -576,32 +574,33 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                 const float* Gj = sG + j * kC;
                 const float* Bj = sBet + j * kC;
                 const float* Yj = sGam + j * kC;
-                if (j == 0) {  // the Gram matrices into shared memory
+                if (j == 0) {  // K K^T into shared memory (Q K^T stays in tensor memory for P)
                     if (!mbar_wait_bounded(&s_bar, phase)) s_fail = 1;
                     umma::fence_after_sync();
-                    const int lr = 32 * (warp & 3) + lane;  // M = 128: row = TMEM lane
-                    float v[32];
-                    umma::tmem_ld32(tG + wl + 32 * (warp >> 2), v);
-                    float* dst = lr < kC ? kk + lr * kLd : qk + (lr - kC) * kLd;
+                    if ((warp & 3) < 2) {  // M = 128: row = TMEM lane; rows 0-63 are K K^T
+                        const int lr = 32 * (warp & 3) + lane;
+                        float v[32];
+                        umma::tmem_ld32(tG + wl + 32 * (warp >> 2), v);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) dst[32 * (warp >> 2) + q] = v[q];
+                        for (int q = 0; q < 32; ++q) kk[lr * kLd + 32 * (warp >> 2) + q] = v[q];
+                    }
                     named_sync(kBarT, kGrp);
                 }
-                // A (strictly lower) and P; lanes along t
-                unsigned char* pimg = ws.kp + rec * kKPBytes + kImgBytes;
+                // A (strictly lower); lanes along t.  The decays first, then the products:
+                // in one fused loop their exponentials were compiled to run one after another.
                 for (int idx = tid; idx < kC * kC / 8; idx += kGrp) {
                     const int t = idx & (kC - 1), s0 = 8 * (idx >> 6);
-                    float pv[8], av[8];
+                    float av[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    if (s0 < t) {
+                        float dec[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = s0 + e;
-                        const float dec = s <= t ? expf(Gj[t] - Gj[s]) : 0.f;
-                        av[e] = s < t ? __fmul_rn(__fmul_rn(Bj[t], dec), kk[t * kLd + s]) : 0.f;
-                        pv[e] = __fmul_rn(dec, qk[t * kLd + s]);
+                        for (int e = 0; e < 8; ++e) dec[e] = expf(Gj[t] - Gj[s0 + e]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            av[e] = s0 + e < t ? __fmul_rn(__fmul_rn(Bj[t], dec[e]), kk[t * kLd + s0 + e]) : 0.f;
                     }
                     *reinterpret_cast<float4*>(Ab + t * kAld + s0) = make_float4(av[0], av[1], av[2], av[3]);
                     *reinterpret_cast<float4*>(Ab + t * kAld + s0 + 4) = make_float4(av[4], av[5], av[6], av[7]);
-                    umma::store_split8(pimg, t, s0, kC, pv);
                 }
                 named_sync(kBarT, kGrp);
                 inverse_blocked(Ab, Tb, reinterpret_cast<float*>(timg), tid, kBarT);
@@ -631,6 +630,7 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                 if (R::bufs == 2 && (j + 1 < f || (j >= 1 && has_next))) cp_async_wait<1>();
                 else cp_async_wait<0>();
                 if (j == 0 && !mbar_wait_bounded(&s_bar, phase)) s_fail = 1;  // the Q image is free once the Gram products are done
+                umma::fence_after_sync();
                 named_sync(kBarV, kGrp);
                 if (first) {
                     fill_conv_state<T>(a, rb, cbv(j), g.dv, n, tb, t0, vt, kGrp);
@@ -647,6 +647,22 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
                     }
                     umma::store_split8(qimg, t, c, g.dv, y0);
                     umma::store_split8(qimg, t + 1, c, g.dv, y1);
+                }
+                // P = decay * Q K^T (s <= t) of this head into the workspace, from the Gram
+                // product's rows 64-127 in tensor memory: warps 10, 11, 14, 15 (the warps of
+                // this group that reach those lanes), one row and 32 columns per thread
+                if ((warp & 3) >= 2) {
+                    const int t = 32 * ((warp & 3) - 2) + lane, c0 = 32 * ((warp - 8) >> 2);
+                    float v[32], dec[32];
+                    umma::tmem_ld32(tG + wl + c0, v);
+                    const float* Gj = sG + j * kC;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) dec[q] = expf(Gj[t] - Gj[c0 + q]);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] = c0 + q <= t ? __fmul_rn(dec[q], v[q]) : 0.f;
+                    unsigned char* pimg = ws.kp + rec * kKPBytes + kImgBytes;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 8) umma::store_split8(pimg, t, c0 + q, kC, v + q);
                 }
                 if (R::bufs == 2 && j + 2 < f) {  // the buffer is free: value head j+2 starts copying
                     named_sync(kBarV, kGrp);
