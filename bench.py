@@ -285,8 +285,52 @@ def run_decode(args, dev, dist, rank, world, st, steps):
     ev_k = [torch.cuda.Event() for _ in range(2)]    # the kernel on set k has finished
     ev_out = [torch.cuda.Event() for _ in range(2)]  # output of set k is back on the host
     used = [False, False]
+    rt = _cudart_calls()
+    if rt is not None:
+        # the same step with the CUDA runtime's copy, event and wait calls made directly (the
+        # runtime already loaded in this process): torch's Python dispatch of those eight calls
+        # per step would take about as long as the kernel on this host
+        memcpy, record, wait, create = rt
+        evs = []
+        for _ in range(6):
+            h = ctypes.c_void_p()
+            if create(ctypes.byref(h), 2):  # cudaEventDisableTiming
+                raise RuntimeError("cudaEventCreateWithFlags failed")
+            evs.append(h)
+        c_in, c_k, c_out = evs[0:2], evs[2:4], evs[4:6]
+        sm, s1, s2 = ctypes.c_void_p(sh), ctypes.c_void_p(s_h2d.cuda_stream), ctypes.c_void_p(s_d2h.cuda_stream)
+        hin = [h.data_ptr() for h in h_in]
+        din, dout, hout = [b.data_ptr() for b in d_in], [o.data_ptr() for o in d_out], [o.data_ptr() for o in h_out]
+        nout = h_out[0].numel() * 4
 
-    def e2e_step(i):
+        def e2e_step(i):
+            j, r, k = i % n_in, i % R, i & 1
+            if used[k]:
+                wait(s1, c_k[k], 0)  # the kernel two steps back is done with d_in[k]
+            e = memcpy(din[k], hin[j], nbytes, 1, s1) or record(c_in[k], s1) or wait(sm, c_in[k], 0)
+            if not e and used[k]:
+                e = wait(sm, c_out[k], 0)  # d_out[k] has been read back
+            if e:
+                raise RuntimeError(f"CUDA runtime error {e} in the e2e step")
+            rc = abi(cfg_ref, B_DECODE, *ptrs[(k, r)], sh)
+            if rc:
+                raise RuntimeError(f"gdn_forward_decode: {gb.gdn_status_string(rc)}")
+            e = record(c_k[k], sm) or wait(s2, c_k[k], 0) or memcpy(hout[k], dout[k], nout, 2, s2) or record(c_out[k], s2)
+            if e:
+                raise RuntimeError(f"CUDA runtime error {e} in the e2e step")
+            used[k] = True
+
+        def drain():
+            for k in range(2):
+                if used[k]:
+                    wait(sm, c_out[k], 0)
+    else:
+        def drain():
+            for k in range(2):
+                if used[k]:
+                    stream.wait_event(ev_out[k])
+
+    def e2e_step_torch(i):
         j, r, k = i % n_in, i % R, i & 1
         if used[k]:
             s_h2d.wait_event(ev_k[k])  # the kernel two steps back is done with d_in[k]
@@ -306,6 +350,8 @@ def run_decode(args, dev, dist, rank, world, st, steps):
             ev_out[k].record(s_d2h)
         used[k] = True
 
+    if rt is None:
+        e2e_step = e2e_step_torch
     for i in range(args.warmup):
         e2e_step(i)
     if dist:
@@ -315,9 +361,7 @@ def run_decode(args, dev, dist, rank, world, st, steps):
     s_h2d.wait_event(e0)
     for i in range(args.steps):
         e2e_step(i)
-    for k in range(2):
-        if used[k]:
-            stream.wait_event(ev_out[k])
+    drain()
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = _max_over_ranks(dist, e0.elapsed_time(e1), dev)
@@ -327,7 +371,26 @@ def run_decode(args, dev, dist, rank, world, st, steps):
                 e2e=None if args.no_e2e else dict(value=_job_value(B_DECODE * args.steps, world, ms_e2e), unit="tokens/s",
                          h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h, overlap="H2D and D2H streams, two buffer sets: copies of "
-                         "neighbouring steps overlap the kernel"), inputs=dict(steps=steps, state=st))
+                         "neighbouring steps overlap the kernel",
+                         host_calls="CUDA runtime via ctypes" if rt is not None else "torch"),
+                inputs=dict(steps=steps, state=st))
+
+
+def _cudart_calls():
+    """cudaMemcpyAsync, cudaEventRecord, cudaStreamWaitEvent and cudaEventCreateWithFlags of the
+    CUDA runtime this process has loaded (torch's and the library's), or None."""
+    import ctypes
+    try:
+        rt = ctypes.CDLL("libcudart.so.13")
+    except OSError:
+        return None
+    vp, c = ctypes.c_void_p, ctypes
+    memcpy, record, wait, create = rt.cudaMemcpyAsync, rt.cudaEventRecord, rt.cudaStreamWaitEvent, rt.cudaEventCreateWithFlags
+    memcpy.argtypes, memcpy.restype = [vp, vp, c.c_size_t, c.c_int, vp], c.c_int
+    record.argtypes, record.restype = [vp, vp], c.c_int
+    wait.argtypes, wait.restype = [vp, vp, c.c_uint], c.c_int
+    create.argtypes, create.restype = [c.POINTER(vp), c.c_uint], c.c_int
+    return memcpy, record, wait, create
 
 
 def _time_calls(fn, reps, flush):
