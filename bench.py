@@ -290,7 +290,7 @@ def run_decode(args, dev, dist, rank, world, st, steps):
         # the same step with the CUDA runtime's copy, event and wait calls made directly (the
         # runtime already loaded in this process): torch's Python dispatch of those eight calls
         # per step would take about as long as the kernel on this host
-        memcpy, record, wait, create = rt
+        memcpy, record, wait, create, devptr = rt
         evs = []
         for _ in range(6):
             h = ctypes.c_void_p()
@@ -367,12 +367,44 @@ def run_decode(args, dev, dist, rank, world, st, steps):
     ms_e2e = _max_over_ranks(dist, e0.elapsed_time(e1), dev)
     h2d = nbytes
     d2h = h_out[0].numel() * 4
+    # The same steps with the kernel reading each step's inputs from, and writing its output
+    # to, the pinned host buffers themselves (NVLink-C2C; device addresses of the pinned
+    # memory from cudaHostGetDevicePointer): every step still moves its own bytes between
+    # host and device, with no copy, event or wait between consecutive launches.
+    ms_zc = None
+    if rt is not None:
+        def dptr(t):
+            p_ = ctypes.c_void_p()
+            return None if devptr(ctypes.byref(p_), ctypes.c_void_p(t.data_ptr()), 0) else p_.value
+        zin, zout = [dptr(h) for h in h_in], [dptr(h) for h in h_out]
+        if all(p_ is not None for p_ in zin + zout):
+            zptrs = {(j, k, r): (zin[j], w.data_ptr(), zin[j] + nq, zin[j] + nq + ng, conv[r].data_ptr(),
+                                 S[r].data_ptr(), zout[k]) for j in range(n_in) for k in range(2) for r in range(R)}
+
+            def zstep(i):
+                rc = abi(cfg_ref, B_DECODE, *zptrs[(i % n_in, i & 1, i % R)], sh)
+                if rc:
+                    raise RuntimeError(f"gdn_forward_decode: {gb.gdn_status_string(rc)}")
+
+            torch.cuda.synchronize()
+            for i in range(args.warmup):
+                zstep(i)
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for i in range(args.steps):
+                zstep(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms_zc = _max_over_ranks(dist, e0.elapsed_time(e1), dev)
     return dict(ms=ms, value=value, launch_us=launch_us, bytes=per_step, rotation=R,
                 e2e=None if args.no_e2e else dict(value=_job_value(B_DECODE * args.steps, world, ms_e2e), unit="tokens/s",
                          h2d_bytes_per_step=h2d,
                          d2h_bytes_per_step=d2h, overlap="H2D and D2H streams, two buffer sets: copies of "
                          "neighbouring steps overlap the kernel",
-                         host_calls="CUDA runtime via ctypes" if rt is not None else "torch"),
+                         host_calls="CUDA runtime via ctypes" if rt is not None else "torch",
+                         zero_copy_value=None if ms_zc is None else _job_value(B_DECODE * args.steps, world, ms_zc)),
                 inputs=dict(steps=steps, state=st))
 
 
@@ -390,7 +422,9 @@ def _cudart_calls():
     record.argtypes, record.restype = [vp, vp], c.c_int
     wait.argtypes, wait.restype = [vp, vp, c.c_uint], c.c_int
     create.argtypes, create.restype = [c.POINTER(vp), c.c_uint], c.c_int
-    return memcpy, record, wait, create
+    devptr = rt.cudaHostGetDevicePointer
+    devptr.argtypes, devptr.restype = [c.POINTER(vp), vp, c.c_uint], c.c_int
+    return memcpy, record, wait, create, devptr
 
 
 def _time_calls(fn, reps, flush):
