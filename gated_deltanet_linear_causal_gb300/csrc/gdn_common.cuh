@@ -113,16 +113,18 @@ struct ConvWindow {
             w[j] = (wi >= 0) ? to_f32(weight[wi]) : 0.f;
         }
     }
-    // Push the next sample; return silu(conv) for the token it completes.
-    __device__ __forceinline__ float push(T v) {
+    // Push the next sample; return the conv sum (before the SiLU) for the token it completes.
+    __device__ __forceinline__ float push_pre(T v) {
 #pragma unroll
         for (int j = 0; j < kMaxConv - 1; ++j) raw[j] = raw[j + 1];
         raw[kMaxConv - 1] = v;
         float acc = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxConv; ++j) acc = fmaf(w[j], to_f32(raw[j]), acc);
-        return silu(acc);
+        return acc;
     }
+    // Push the next sample; return silu(conv) for the token it completes.
+    __device__ __forceinline__ float push(T v) { return silu(push_pre(v)); }
     // Write the K-1 sample conv state after the last push (oldest first) to dst.
     // Loop bounds and register indices are compile-time: the window stays in
     // registers.

@@ -373,10 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                     T xt[CG];
 #pragma unroll
                     for (int u = 0; u < CG; ++u) xt[u] = qkv[((size_t)b * g.D + cc[u]) * L + t];
+                    // the group's conv sums, then their SiLUs in passes (fast intrinsics): one
+                    // SiLU per channel in turn ran as a chain of special-function latencies
+                    float pre[CG], yv[CG];
+#pragma unroll
+                    for (int u = 0; u < CG; ++u) pre[u] = win[u].push_pre(xt[u]);
+                    silu_fast_n(pre, yv);
 #pragma unroll
                     for (int u = 0; u < CG; ++u) {
                         const int ch = ch0 + u;
-                        const float y = win[u].push(xt[u]);
+                        const float y = yv[u];
                         if (ch < 2 * DK) qk[t * 2 * DK + ch] = y;
                         else vv[t * fi * g.dv + (ch - 2 * DK)] = y;
                         if (!IN_PLACE && (qk_snap || ch >= 2 * DK))
@@ -407,25 +413,40 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                 put_ab(idx, a.gate[gi], a.beta[gi]);
             }
             named_sync(kBarProlog, kProlog);
-            for (int t = 0; t < L; ++t) {
-                float sq = 0.f, sk = 0.f, skq = 0.f;
-                for (int e = pt; e < DK; e += kProlog) {
-                    const float qv = qk[t * 2 * DK + e], kv = qk[t * 2 * DK + DK + e];
-                    sq = fmaf(qv, qv, sq);
-                    sk = fmaf(kv, kv, sk);
-                    skq = fmaf(kv, qv, skq);
+            // verify: the tokens' partial sums four at a time, then their shuffle reductions
+            // together (twelve independent chains instead of three per token in turn); each sum
+            // runs in the same order as token by token.  Decode has one token.
+            constexpr int TG = IN_PLACE ? 1 : 4;
+            for (int t0 = 0; t0 < L; t0 += TG) {
+                float sq[TG], sk[TG], skq[TG];
+#pragma unroll
+                for (int dt = 0; dt < TG; ++dt) {
+                    sq[dt] = sk[dt] = skq[dt] = 0.f;
+                    if (t0 + dt < L)
+                        for (int e = pt; e < DK; e += kProlog) {
+                            const int t = t0 + dt;
+                            const float qv = qk[t * 2 * DK + e], kv = qk[t * 2 * DK + DK + e];
+                            sq[dt] = fmaf(qv, qv, sq[dt]);
+                            sk[dt] = fmaf(kv, kv, sk[dt]);
+                            skq[dt] = fmaf(kv, qv, skq[dt]);
+                        }
                 }
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
-                    skq += __shfl_xor_sync(0xffffffffu, skq, off);
-                }
-                if (lane == 0) {
-                    nred[pw * 3 * kMaxVerify + 3 * t + 0] = sq;
-                    nred[pw * 3 * kMaxVerify + 3 * t + 1] = sk;
-                    nred[pw * 3 * kMaxVerify + 3 * t + 2] = skq;
-                }
+                for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+                    for (int dt = 0; dt < TG; ++dt) {
+                        sq[dt] += __shfl_xor_sync(0xffffffffu, sq[dt], off);
+                        sk[dt] += __shfl_xor_sync(0xffffffffu, sk[dt], off);
+                        skq[dt] += __shfl_xor_sync(0xffffffffu, skq[dt], off);
+                    }
+                if (lane == 0)
+#pragma unroll
+                    for (int dt = 0; dt < TG; ++dt)
+                        if (t0 + dt < L) {
+                            nred[pw * 3 * kMaxVerify + 3 * (t0 + dt) + 0] = sq[dt];
+                            nred[pw * 3 * kMaxVerify + 3 * (t0 + dt) + 1] = sk[dt];
+                            nred[pw * 3 * kMaxVerify + 3 * (t0 + dt) + 2] = skq[dt];
+                        }
             }
             named_sync(kBarProlog, kProlog);
             if (pt < L) {
