@@ -7,7 +7,17 @@
 
 namespace gdn {
 
-constexpr uint32_t kWaitLimit = 1u << 23;  // polls before a wait is declared stuck
+// A wait that has not ended after this long has failed (every wait here is for a copy,
+// an MMA or a peer CTA of the same kernel, which take microseconds).  The limit is a
+// time, read from the global timer, because one poll of an mbarrier may suspend the
+// thread for a varying, system-dependent time (several microseconds measured here).
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -72,21 +82,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; false after kWaitLimit polls.
+// Wait for phase `parity` of `bar` to complete; false once kWaitNs have passed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
 }
 
 // Like mbar_wait_bounded, but also gives up as soon as *abort becomes nonzero
 // (another role of the CTA has given up and will never complete the phase).
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-    }
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (*abort || global_ns() - t0 > kWaitNs) return false;
+    return true;
 }
 
 // ---- distributed shared memory (thread-block clusters) ----------------------
@@ -105,21 +117,25 @@ __device__ __forceinline__ void st_async_cluster(uint32_t addr, float v, uint32_
                  "r"(bar_addr)
                  : "memory");
 }
-// Wait (acquire at cluster scope) for phase `parity` of a local mbarrier that other
-// CTAs of the cluster arrive on; false after kWaitLimit polls or once *abort is set.
+// One poll (acquire at cluster scope) of phase `parity` of a local mbarrier that other
+// CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for that phase; false once kWaitNs have passed or once *abort (if given) is set.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if (abort && *abort) return false;
-    }
-    return false;
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_cluster(bar, parity))
+        if ((abort && *abort) || global_ns() - t0 > kWaitNs) return false;
+    return true;
 }
 
 // Arrive on named barrier `id` without waiting (the barrier completes when `count`
