@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -45,10 +46,24 @@ def _peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|/\*.*?\*/|//[^\n]*|\s+', re.S)
+
+
+def _code_only(text):
+    """Source text with comments removed and every run of whitespace made one space (string
+    literals otherwise kept), so that an edit to comments or layout does not count as a change
+    of the kernel."""
+    def keep(m):
+        t = m.group(0)
+        return t if t.startswith('"') else " "
+    return re.sub(r"\s+", " ", _CODE_TOKENS.sub(keep, text)).strip()
+
+
 def _source_sha(names):
     h = hashlib.sha256()
     for n in names:
-        h.update(open(os.path.join(ROOT, "gated_deltanet_linear_causal_gb300", "csrc", n), "rb").read())
+        with open(os.path.join(ROOT, "gated_deltanet_linear_causal_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

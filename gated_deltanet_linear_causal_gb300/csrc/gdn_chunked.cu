@@ -731,8 +731,8 @@ __global__ void __launch_bounds__(kPT, 1) chunk_prep_kernel(const PrefillArgs a,
     if (warp == 0) umma::tmem_free(s_tmem, 512);
 }
 
-// 32 consecutive values of the io type (16-byte aligned) to and from fp32.
-// The 32 values of a row of io type T held as raw 16-byte words (4 for bf16, 8 for fp32).
+// 32 consecutive values of the io type as fp32: from raw 16-byte words (4 for bf16, 8 for
+// fp32) already loaded, and to a 16-byte aligned row.
 template <typename T>
 __device__ __forceinline__ void unpack_row32(const uint4 (&r)[32 * sizeof(T) / 16], float (&v)[32]) {
     if constexpr (sizeof(T) == 2) {
