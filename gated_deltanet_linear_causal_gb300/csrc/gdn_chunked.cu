@@ -788,10 +788,10 @@ __device__ __forceinline__ void tmem_pair(uint32_t taddr, float (&v)[kNS]) {
 //   round B   MMA  K~_c^T U -> tS;  [P_c; P_c] U accumulated onto tA[b], so rows
 //             64-127 become O = Q~ S0 + P U (rows 0-63 are spent)
 //             all: S0 <- gamma_last S0 + tS -> S0 image
-// Copies run ahead (issued by one thread of the output warps, so that the MMA
-// issuer never waits on them): W/Q~ double-buffered two chunks ahead (free once round A of
-// the chunk before has completed), K~ once K~^T U has completed, u once the U
-// rows have been read, and P (twice, for the stacked operand) once P U has.
+// Copies run ahead (issued by two threads of warps 2-3, so that the MMA issuer never
+// waits on them): W/Q~ double-buffered two chunks ahead (issued in round A, once round A
+// of the chunk has completed and freed its buffer), K~ once K~^T U has completed, u once
+// the U rows have been read, and P (twice, for the stacked operand) once P U has.
 // NORM: the gated RMSNorm of section 2 is applied to the output rows.  That work
 // (sums of squares, SiLU of z, the stores) is too long for warps 2-3's share of round
 // A, so warps 6-7 (the same TMEM lanes) take the output rows instead, outside the
@@ -903,9 +903,11 @@ __global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const Prefi
     const uint32_t tS = tmem, tA0 = tmem + 64;      // tA[b] = tA0 + 64 b
     const uint32_t wl = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes = accumulator rows 32 warp ..
 
-    // Thread kIssuer issues the MMAs, thread kCopier the bulk copies; each counts what it
+    // Thread kIssuer issues the MMAs, threads kCopier and kCopierWQ the bulk copies (one
+    // thread issues a bulk copy only every few hundred cycles, so the W/Q~ copies go to a
+    // second thread, in round A, off the path to the end of the chunk); each counts what it
     // issued per barrier (for a clean exit on abort).
-    constexpr int kCopier = 64;
+    constexpr int kCopier = 64, kCopierWQ = 96;
     int wq_iss[2] = {0, 0}, u_iss = 0, k_iss = 0, p_iss = 0, a_iss = 0, b_iss = 0;
     auto rec = [&](int c) { return (size_t)(chunk0 + c) * g.Hv + h; };
     auto load_wq = [&](int c) {
@@ -1026,9 +1028,11 @@ __global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const Prefi
     if (NORM && warp >= kCT / 32) {
         if (warp >= 6) norm_rows();
     } else {
-    if (tid == kCopier) {
+    if (tid == kCopierWQ) {
         load_wq(0);
         if (nch > 1) load_wq(1);
+    }
+    if (tid == kCopier) {
         load_u(0);
         load_k(0);
         load_p(0);
@@ -1054,6 +1058,10 @@ __global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const Prefi
                 else if (tid == kCopier)
                     wait_all(&s_o, (uint32_t)((c - 1) & 1));
                 if (tid == kCopier) load_p(c);  // P U of chunk c-1 has completed: the P buffer is free
+            }
+            if (tid == kCopierWQ && c + 2 < nch) {
+                wait_all(&s_a, (uint32_t)(c & 1));  // round A of chunk c has completed: its W/Q~ buffer is free
+                load_wq(c + 2);
             }
         } else if (warp < 2) {  // U = u - X, rows 0-63
             wait_all(&s_a, (uint32_t)(c & 1));
@@ -1094,6 +1102,7 @@ __global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const Prefi
         }
         if (srow) {
             wait_all(&s_s, (uint32_t)(c & 1));
+            if (tid == kCopier && c + 1 < nch) load_k(c + 1);  // K~^T U has completed: the K~ buffer is free
             umma::fence_after_sync();
             float ss[kNS];
             tmem_pair(tS + wl, ss);
@@ -1101,10 +1110,6 @@ __global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const Prefi
             for (int j = 0; j < kNS; ++j) S[j] = fmaf(glc, S[j], ss[j]);
 #pragma unroll
             for (int j = 0; j < kNS; j += 8) umma::store_split8(s0t, tid, j, kNS, S + j);
-        }
-        if (tid == kCopier) {
-            if (c + 2 < nch) load_wq(c + 2);  // round A of chunk c has completed: its W/Q~ buffer is free
-            if (c + 1 < nch) load_k(c + 1);   // and K~^T U: the K~ buffer is free
         }
         fence_proxy_async_smem();
         umma::fence_before_sync();
@@ -1117,9 +1122,10 @@ __global__ void __launch_bounds__(NORM ? kCTN : kCT, 1) chain_kernel(const Prefi
     // on abort, let copies and MMAs still in flight land before TMEM and shared memory
     // are released: wait for the last issued phase of each barrier (a completed phase
     // returns at once)
-    if (s_abort && tid == kCopier) {
+    if (s_abort && tid == kCopierWQ)
         for (int b = 0; b < 2; ++b)
             if (wq_iss[b]) mbar_wait_bounded(&s_wq[b], (uint32_t)((wq_iss[b] - 1) & 1));
+    if (s_abort && tid == kCopier) {
         if (u_iss) mbar_wait_bounded(&s_u, (uint32_t)((u_iss - 1) & 1));
         if (k_iss) mbar_wait_bounded(&s_k, (uint32_t)((k_iss - 1) & 1));
         if (p_iss) mbar_wait_bounded(&s_p, (uint32_t)((p_iss - 1) & 1));
