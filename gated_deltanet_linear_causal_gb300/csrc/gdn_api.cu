@@ -67,7 +67,7 @@ const char* gdn_status_string(gdn_status_t s) {
         case GDN_ERR_SEQLENS: return "cu_seqlens must start at 0 and be non-decreasing";
         case GDN_ERR_CUDA: return "CUDA launch failed";
         case GDN_ERR_DEVICE_TIMEOUT: return "bounded device-side wait gave up";
-        case GDN_ERR_UNSUPPORTED: return "shape or variant not supported by this build";
+        case GDN_ERR_UNSUPPORTED: return "shape or variant not supported by this library";
         case GDN_ERR_WORKSPACE: return "workspace missing or too small";
         case GDN_ERR_RANGE: return "accepted length outside [0, L]";
     }
