@@ -322,6 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
         const T* cin = static_cast<const T*>(a.conv_in);
         T* cout = static_cast<T*>(a.conv_out);
         const int nch = 2 * DK + fi * g.dv;
+        // the grouped conv-window loads below: bf16, K = 4, and every group's 24 state bytes
+        // 8-byte aligned and 32 weight bytes 16-byte aligned (channel groups start at
+        // multiples of 4, so D % 4 == 0 and aligned bases suffice)
+        const bool vec_conv = sizeof(T) == 2 && kStreamConv == 4 && g.K == 4 && g.D % 4 == 0 &&
+                              (reinterpret_cast<uintptr_t>(cin) & 7) == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0;
         for (int i = 0; i < my_items; ++i) {
             const int buf = i & 1;
             if (!mbar_wait_or_abort(qempty + buf, (uint32_t)(((i >> 1) & 1) ^ 1), &s_abort)) s_pabort = 1;
@@ -367,7 +372,29 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const StepArgs a, c
                     cc[u] = ch < DK ? hk * DK + ch
                           : ch < 2 * DK ? g.Hk * DK + hk * DK + (ch - DK)
                                         : 2 * g.Hk * DK + h0 * g.dv + (ch - 2 * DK);
-                    win[u].load(cin + ((size_t)b * g.D + cc[u]) * (g.K - 1), w + (size_t)cc[u] * g.K, g.K);
+                }
+                if (vec_conv) {
+                    // bf16, K = 4: the group's 4 x 3 state samples (24 bytes) and 4 x 4 taps
+                    // (32 bytes) are contiguous, so they come in 3 + 2 wide loads instead of
+                    // 28 scalar ones; the windows hold exactly what load() would put there
+                    const uint2* sp = reinterpret_cast<const uint2*>(cin + ((size_t)b * g.D + cc[0]) * 3);
+                    const uint4* wp = reinterpret_cast<const uint4*>(w + (size_t)cc[0] * 4);
+                    const uint2 sv[3] = {sp[0], sp[1], sp[2]};
+                    const uint4 wv[2] = {wp[0], wp[1]};
+                    const T* sb = reinterpret_cast<const T*>(sv);
+                    const T* wb = reinterpret_cast<const T*>(wv);
+#pragma unroll
+                    for (int u = 0; u < CG; ++u) {
+                        win[u].raw[0] = zero_elem<T>();
+#pragma unroll
+                        for (int j = 0; j < 3; ++j) win[u].raw[1 + j] = sb[3 * u + j];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) win[u].w[j] = to_f32(wb[4 * u + j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < CG; ++u)
+                        win[u].load(cin + ((size_t)b * g.D + cc[u]) * (g.K - 1), w + (size_t)cc[u] * g.K, g.K);
                 }
                 for (int t = 0; t < L; ++t) {
                     T xt[CG];
