@@ -150,3 +150,31 @@ def test_gated_norm_and_gated_decode_validation(lib):
     p[7] = FAKE + 4
     assert dg(cfg, ptrs=p) == 3                                # norm weight not 16-byte aligned
     assert dg(cfg, y=FAKE + 2) == 3
+
+
+def test_prefill_gated_validation(lib):
+    cfg = _cfg()
+    F = ctypes.c_float
+
+    # gdn_forward_prefill_gated(cfg, N, cu, cu_host, qkv, w, gate, beta, conv, S, z, norm_w, eps, y,
+    #                           variant, workspace, workspace_bytes, stream)
+    def call(c=cfg, cu=(0, 64), eps=1e-6, z=FAKE, wgt=FAKE, y=FAKE, variant=0, ws_bytes=16, n=None):
+        cu = np.ascontiguousarray(cu, np.int32)
+        n = len(cu) - 1 if n is None else n
+        return lib.gdn_forward_prefill_gated(ctypes.byref(c), n, FAKE, cu.ctypes.data, *[FAKE] * 6, z, wgt, F(eps), y,
+                                             variant, FAKE, ws_bytes, None)
+
+    assert call(eps=-1.0) == 2                                 # eps must be >= 0 and finite
+    assert call(eps=float("inf")) == 2
+    assert call(z=0) == 1 and call(wgt=0) == 1 and call(y=0) == 1
+    assert call(n=0) == 0                                      # no sequences: no-op
+    assert call(cu=(0, 0)) == 0                                # T = 0: no-op
+    assert call(cu=(1, 64)) == 5                               # cu_seqlens must start at 0
+    assert call(y=FAKE + 8) == 3                               # y, z and the weight 16-byte aligned
+    assert call(z=FAKE + 4) == 3
+    assert call(wgt=FAKE + 4) == 3
+    # the CTAs of a value head form one cluster of at most 8: d_v <= 128 in both forms
+    assert call(c=_cfg(head_v_dim=256)) == 8
+    assert call(c=_cfg(head_v_dim=256), variant=1) == 8
+    assert call(ws_bytes=16) == 9                              # workspace too small (checked last)
+    assert call(variant=1, ws_bytes=16) == 9
